@@ -1,0 +1,309 @@
+"""Pins of the float64 oracle against facts that do not come from the oracle
+itself: values printed or fixed by the pages, closed forms, invariants,
+brute force on a toy, and special cases that reduce to something simpler.
+
+CPU only (no GPU needed)."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import mla_oracle as O
+from sparse_latent_attention_decode_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_pairs(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split()
+            vals[k] = v
+    return vals
+
+
+ARGS = _read_pairs("model_args_defaults.txt")
+ROPE_KW = dict(rope_dim=int(ARGS["qk_rope_head_dim"]), rope_theta=float(ARGS["rope_theta"]),
+               rope_factor=float(ARGS["rope_factor"]), beta_fast=float(ARGS["beta_fast"]),
+               beta_slow=float(ARGS["beta_slow"]), original_seq_len=int(ARGS["original_seq_len"]),
+               max_seq_len=int(ARGS["max_seq_len"]))
+
+
+def _f64(t):
+    return synth.to_f64(t)
+
+
+# ---------------------------------------------------------------- frequencies
+def test_yarn_correction_range_matches_hand_derivation():
+    g = _read_pairs("yarn_inv_freq_closed_form.txt")
+    low, high = O.yarn_correction_range(32, 1, 64, 10000.0, 4096)
+    assert (low, high) == (int(g["low"]), int(g["high"]))
+
+
+def test_yarn_inv_freq_closed_form_values():
+    g = _read_pairs("yarn_inv_freq_closed_form.txt")
+    f = O.yarn_inv_freq(**ROPE_KW)
+    assert f.shape == (32,)
+    for k, v in g.items():
+        if k in ("low", "high"):
+            continue
+        assert f[int(k)] == pytest.approx(float(v), rel=1e-14), k
+
+
+def test_yarn_inv_freq_piecewise_closed_form_all_pairs():
+    # unchanged below the ramp, divided by the factor above it, linear blend between
+    f = O.yarn_inv_freq(**ROPE_KW)
+    for i in range(32):
+        base = 10.0 ** (-i / 8.0)
+        if i <= 10:
+            want = base
+        elif i >= 23:
+            want = base / 40.0
+        else:
+            want = base * ((i - 10) / 520.0 + (23 - i) / 13.0)
+        assert f[i] == pytest.approx(want, rel=1e-13), i
+
+
+def test_no_yarn_when_context_not_extended():
+    kw = dict(ROPE_KW, max_seq_len=4096)
+    f = O.yarn_inv_freq(**kw)
+    np.testing.assert_allclose(f, 10.0 ** (-np.arange(32) / 8.0), rtol=1e-14)
+
+
+def test_softmax_scale_closed_form():
+    g = _read_pairs("softmax_scale_closed_form.txt")
+    assert O.softmax_scale() == pytest.approx(float(g["softmax_scale"]), rel=1e-15)
+    assert O.softmax_scale(max_seq_len=4096) == pytest.approx(float(g["softmax_scale_no_yarn"]), rel=1e-15)
+    assert O.softmax_scale(max_seq_len=4096) == pytest.approx(1.0 / math.sqrt(192.0), rel=1e-15)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_unit_vector_lands_on_cos_sin_interleaved():
+    # e_{2i} rotated by angle th must become (cos th, sin th) in slots (2i, 2i+1):
+    # pins the interleaved pairing and the sign of the rotation
+    f = O.yarn_inv_freq(**ROPE_KW)
+    t = 16383
+    for i in (0, 5, 10, 17, 31):
+        x = np.zeros(64)
+        x[2 * i] = 1.0
+        y = O.rope_interleaved(x, O.freqs_cis([t], f)[0])
+        th = t * f[i]
+        assert y[2 * i] == pytest.approx(math.cos(th), abs=1e-12)
+        assert y[2 * i + 1] == pytest.approx(math.sin(th), abs=1e-12)
+        rest = np.delete(y, [2 * i, 2 * i + 1])
+        assert np.all(rest == 0.0)
+        # the odd slot rotates the other way round: e_{2i+1} -> (-sin, cos)
+        x = np.zeros(64)
+        x[2 * i + 1] = 1.0
+        y = O.rope_interleaved(x, O.freqs_cis([t], f)[0])
+        assert y[2 * i] == pytest.approx(-math.sin(th), abs=1e-12)
+        assert y[2 * i + 1] == pytest.approx(math.cos(th), abs=1e-12)
+
+
+def test_rope_preserves_pair_norms_and_identity_at_zero():
+    rng = np.random.default_rng(0)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    x = rng.standard_normal((7, 128, 64))
+    pos = np.array([0, 1, 999, 1000, 4095, 8191, 16383])
+    y = O.rope_interleaved(x, O.freqs_cis(pos, f)[:, None, :])
+    nx = np.hypot(x[..., 0::2], x[..., 1::2])
+    ny = np.hypot(y[..., 0::2], y[..., 1::2])
+    np.testing.assert_allclose(ny, nx, rtol=1e-13)
+    np.testing.assert_array_equal(y[0], x[0])
+
+
+def test_rope_composition_law():
+    f = O.yarn_inv_freq(**ROPE_KW)
+    a, b = 1234, 15000 - 1234
+    ca, cb, cab = O.freqs_cis([a], f)[0], O.freqs_cis([b], f)[0], O.freqs_cis([a + b], f)[0]
+    np.testing.assert_allclose(ca * cb, cab, atol=1e-11)
+
+
+def test_rope_low_pairs_rotate_by_unscaled_frequency():
+    # pairs i <= 10 sit below the YaRN ramp: angle = t * 10000^(-i/32)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    t = 16383
+    c = O.freqs_cis([t], f)[0]
+    for i in range(11):
+        th = t * 10000.0 ** (-i / 32.0)
+        assert c[i] == pytest.approx(complex(math.cos(th), math.sin(th)), abs=1e-10)
+
+
+# ---------------------------------------------------------------- attention
+def _small_case(B=2, end_pos=(300, 257), k=100, S_cap=320, seed=1, selection="uniform"):
+    wl = synth.small_workload(B, list(end_pos), k=k, K=k, S_cap=S_cap, selection=selection)
+    t = synth.make_inputs(wl, seed=seed)
+    return wl, {n: _f64(v) for n, v in t.items()}
+
+
+def test_worked_example_shapes():
+    g = _read_pairs("worked_example_p1000.txt")
+    wl = synth.workload("p1000_b1")
+    assert wl.end_pos[0] == int(g["keys_read"]) == int(g["cached_positions"]) + 1
+    x = {n: _f64(v) for n, v in synth.make_inputs(wl).items()}
+    f = O.yarn_inv_freq(**ROPE_KW)
+    q_lat = O.q_latent(x["q_nope"], x["q_pe"], x["wkv_b"], x["end_pos"], f)
+    assert q_lat.shape == (1, int(g["heads"]), int(g["q_width"]))
+    assert x["kv_cache"].shape[-1] + x["pe_cache"].shape[-1] == int(g["k_width"])
+    _, p = O.attend_one(q_lat[0, :, :512], q_lat[0, :, 512:], x["kv_cache"][0], x["pe_cache"][0],
+                        x["topk_idx"][0], int(x["end_pos"][0]), O.softmax_scale(), return_probs=True)
+    assert p.shape == (int(g["heads"]), int(g["keys_read"]))
+
+
+def test_softmax_rows_sum_to_one():
+    wl, x = _small_case()
+    f = O.yarn_inv_freq(**ROPE_KW)
+    q_lat = O.q_latent(x["q_nope"], x["q_pe"], x["wkv_b"], x["end_pos"], f)
+    for b in range(wl.B):
+        _, p = O.attend_one(q_lat[b, :, :512], q_lat[b, :, 512:], x["kv_cache"][b], x["pe_cache"][b],
+                            x["topk_idx"][b], wl.end_pos[b], O.softmax_scale(), return_probs=True)
+        np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-12)
+        unsel = np.ones(wl.end_pos[b], bool)
+        unsel[x["topk_idx"][b][x["topk_idx"][b] >= 0]] = False
+        assert np.all(p[:, unsel] == 0.0)
+
+
+def test_absorbed_equals_naive_non_absorbed_at_p1000():
+    # the pages' worked example (1001 keys, all selected): absorbing W_UK into the
+    # query and W_UV into the output must equal ordinary per-head attention over
+    # keys/values expanded from the latent cache
+    wl = synth.workload("p1000_b1")
+    x = {n: _f64(v) for n, v in synth.make_inputs(wl).items()}
+    f = O.yarn_inv_freq(**ROPE_KW)
+    s = O.softmax_scale()
+    out = O.decode_step(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                        x["topk_idx"], x["end_pos"], f, s)
+    q_pe_rot = O.rope_for_batch(x["q_pe"], x["end_pos"], f)
+    naive = O.naive_attention_one(x["q_nope"][0], q_pe_rot[0], x["kv_cache"][0], x["pe_cache"][0],
+                                  x["wkv_b"], x["topk_idx"][0], 1001, s)
+    np.testing.assert_allclose(out[0], naive, rtol=0, atol=1e-12 * np.abs(naive).max())
+
+
+def test_absorbed_equals_naive_with_sparse_selection():
+    wl, x = _small_case(B=1, end_pos=(300,), k=37)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    s = O.softmax_scale()
+    out = O.decode_step(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                        x["topk_idx"], x["end_pos"], f, s)
+    q_pe_rot = O.rope_for_batch(x["q_pe"], x["end_pos"], f)
+    naive = O.naive_attention_one(x["q_nope"][0], q_pe_rot[0], x["kv_cache"][0], x["pe_cache"][0],
+                                  x["wkv_b"], x["topk_idx"][0], 300, s)
+    np.testing.assert_allclose(out[0], naive, rtol=0, atol=1e-12 * np.abs(naive).max())
+
+
+def test_brute_force_toy_4_heads_8_keys():
+    rng = np.random.default_rng(3)
+    q_lat = rng.standard_normal((128, 576))
+    kv = rng.standard_normal((8, 512))
+    pe = rng.standard_normal((8, 64))
+    topk = np.array([6, 1, -1, 3, 7, 0, 8, 4])   # -1 and 8 are padding for end_pos = 8
+    s = O.softmax_scale()
+    o = O.attend_one(q_lat[:, :512], q_lat[:, 512:], kv, pe, topk, 8, s)
+    bf = O.brute_force_toy(q_lat, kv, pe, topk, 8, s, heads=range(4))
+    for h in range(4):
+        np.testing.assert_allclose(o[h], bf[h], rtol=0, atol=1e-13)
+
+
+def test_single_selected_key_gives_value_projection_of_that_row():
+    wl, x = _small_case(B=1, end_pos=(300,), k=1)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    out = O.decode_step(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                        x["topk_idx"], x["end_pos"], f, O.softmax_scale())
+    t = int(x["topk_idx"][0][0])
+    w_uv = x["wkv_b"].reshape(128, 256, 512)[:, 128:, :]
+    want = np.einsum("hdc,c->hd", w_uv, x["kv_cache"][0][t])
+    np.testing.assert_allclose(out[0], want, rtol=0, atol=1e-12 * np.abs(want).max())
+
+
+def test_zero_query_averages_selected_rows():
+    wl, x = _small_case(B=1, end_pos=(300,), k=50)
+    x["q_nope"][:] = 0.0
+    x["q_pe"][:] = 0.0
+    f = O.yarn_inv_freq(**ROPE_KW)
+    out = O.decode_step(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                        x["topk_idx"], x["end_pos"], f, O.softmax_scale())
+    sel = x["topk_idx"][0]
+    mean = x["kv_cache"][0][sel].mean(axis=0)
+    w_uv = x["wkv_b"].reshape(128, 256, 512)[:, 128:, :]
+    want = np.einsum("hdc,c->hd", w_uv, mean)
+    np.testing.assert_allclose(out[0], want, rtol=0, atol=1e-12 * np.abs(want).max())
+
+
+def test_permutation_duplicates_padding_and_nan_poison():
+    wl, x = _small_case(B=1, end_pos=(300,), k=64)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    s = O.softmax_scale()
+    q_lat = O.q_latent(x["q_nope"], x["q_pe"], x["wkv_b"], x["end_pos"], f)
+    args = (q_lat[0, :, :512], q_lat[0, :, 512:], x["kv_cache"][0], x["pe_cache"][0])
+    row = x["topk_idx"][0]
+    base = O.attend_one(*args, row, 300, s)
+    perm = np.random.default_rng(5).permutation(row)
+    np.testing.assert_allclose(O.attend_one(*args, perm, 300, s), base, rtol=0, atol=1e-14)
+    dup = np.concatenate([row, row[:10], [-1, -7, 300, 10 ** 6]])
+    np.testing.assert_allclose(O.attend_one(*args, dup, 300, s), base, rtol=0, atol=1e-14)
+    kv = x["kv_cache"][0].copy()
+    pe = x["pe_cache"][0].copy()
+    unsel = np.ones(kv.shape[0], bool)
+    unsel[row] = False
+    kv[unsel] = np.nan
+    pe[unsel] = np.nan
+    # scores of unselected keys are NaN here, so compute through the selected rows only
+    sub = O.attend_one(args[0], args[1], kv[row], pe[row], np.arange(64), 64, s)
+    np.testing.assert_allclose(sub, base, rtol=0, atol=1e-13)
+
+
+def test_sparse_equals_dense_over_gathered_subcache():
+    wl, x = _small_case(B=1, end_pos=(300,), k=80)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    s = O.softmax_scale()
+    q_lat = O.q_latent(x["q_nope"], x["q_pe"], x["wkv_b"], x["end_pos"], f)
+    row = x["topk_idx"][0]
+    base = O.attend_one(q_lat[0, :, :512], q_lat[0, :, 512:], x["kv_cache"][0], x["pe_cache"][0], row, 300, s)
+    # plain dense softmax attention (no mask) over the gathered rows
+    kv = x["kv_cache"][0][row]
+    pe = x["pe_cache"][0][row]
+    sc = (q_lat[0, :, :512] @ kv.T + q_lat[0, :, 512:] @ pe.T) * s
+    p = np.exp(sc - sc.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(p @ kv, base, rtol=0, atol=1e-13)
+
+
+def test_empty_selection_gives_zero():
+    wl, x = _small_case(B=1, end_pos=(300,), k=10)
+    row = np.full(10, -1)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    q_lat = O.q_latent(x["q_nope"], x["q_pe"], x["wkv_b"], x["end_pos"], f)
+    o = O.attend_one(q_lat[0, :, :512], q_lat[0, :, 512:], x["kv_cache"][0], x["pe_cache"][0], row, 300,
+                     O.softmax_scale())
+    assert np.all(o == 0.0)
+
+
+# ------------------------------------------------- planted mistakes must be caught
+def test_pins_catch_swapped_weight_halves(monkeypatch):
+    wl, x = _small_case(B=1, end_pos=(300,), k=37)
+    f = O.yarn_inv_freq(**ROPE_KW)
+    s = O.softmax_scale()
+    q_pe_rot = O.rope_for_batch(x["q_pe"], x["end_pos"], f)
+    naive = O.naive_attention_one(x["q_nope"][0], q_pe_rot[0], x["kv_cache"][0], x["pe_cache"][0],
+                                  x["wkv_b"], x["topk_idx"][0], 300, s)
+    real_split = O.split_wkv_b
+    monkeypatch.setattr(O, "split_wkv_b", lambda w: real_split(w)[::-1])
+    bad = O.decode_step(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                        x["topk_idx"], x["end_pos"], f, s)
+    monkeypatch.setattr(O, "split_wkv_b", real_split)
+    assert np.abs(bad[0] - naive).max() > 1e-3 * np.abs(naive).max()
+
+
+def test_pins_catch_non_interleaved_pairing(monkeypatch):
+    def half_split(x, cis):
+        z = x[..., :32] + 1j * x[..., 32:]
+        y = z * cis
+        return np.concatenate([y.real, y.imag], axis=-1)
+    monkeypatch.setattr(O, "rope_interleaved", half_split)
+    with pytest.raises(AssertionError):
+        test_rope_unit_vector_lands_on_cos_sin_interleaved()
