@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step of absorbed, top-k-sparse latent attention.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is the whole path for one batch: RoPE + key absorption
+(mla_absorb_q), then scores / softmax / PV / value up-projection
+(mla_sparse_decode with wkv_b).  Inputs are seeded synthetic tensors already
+resident in HBM; L2 is flushed (a 256 MiB write) before every timed step and
+each step is timed with its own CUDA events on the launching stream.
+
+With N > 1 (torchrun, one process per GPU) each rank runs an independent
+replica on its own batch (different seed): no collective on the data path,
+weak scaling; a barrier and a max-over-ranks reduction bracket the timing.
+
+The line printed by rank 0 also carries: the end-to-end figure through the
+host-buffer API (pinned host inputs copied in, head outputs copied back), the
+roofline of the attention kernel, the float64 oracle timed on a bounded sample
+on the host cores (cpu_baseline), GPU clocks sampled during the timed region,
+and the number of library kernels launched in the timed region.
+
+--impl reference times the float64 CPU oracle (the only reference this path
+has) on the same workload: each step is one sequence of the batch.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "decode query-tokens/sec and achieved HBM GB/s, % of roofline (sparse MLA)"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "sparse_b64_ctx16384_top2048"
+ROW_BYTES = (512 + 64) * 2          # one gathered cache row (latent + rotary), bf16
+FLUSH_BYTES = 256 << 20             # > 126 MB L2
+FALLBACK_HBM_GBS = 6400.0
+
+
+# ----------------------------------------------------------------- distributed plumbing
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (control plane only)."""
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(rank: int, base: int = 0) -> int:
+    """Each rank draws an independent batch of the same shape."""
+    return base + 1000003 * rank
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of the bench GPU during the timed region."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            self.bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}"
+        except Exception:
+            self.bus = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 10:
+                    continue
+                if self.bus and not f[1].upper().endswith(self.bus[-7:]):
+                    continue
+                rows.append(f)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return json.load(open(p))
+    except Exception:
+        return {}
+
+
+def traffic_record(kernel_src: str) -> float | None:
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the kernel source as it is now."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    if rec.get("kernel_source_sha256") != sha:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def selected_rows(topk: torch.Tensor, end_pos: torch.Tensor) -> int:
+    e = end_pos.view(-1, 1).to(topk.device)
+    return int(((topk >= 0) & (topk < e)).sum().item())
+
+
+def oracle_sample(t: dict, wl, budget_s: float, max_seqs: int | None = None):
+    """Time the float64 oracle's full step on sequences 0, 1, ... until the
+    budget is used (at least one).  Returns (sequences, seconds)."""
+    from oracle import mla_oracle as O
+    from sparse_latent_attention_decode_b300 import synth
+    inv = O.yarn_inv_freq()
+    scale = O.softmax_scale()
+    wkv = synth.to_f64(t["wkv_b"])
+    done, spent = 0, 0.0
+    limit = wl.B if max_seqs is None else min(wl.B, max_seqs)
+    while done < limit and (done == 0 or spent < budget_s):
+        b = done
+        x = {k: synth.to_f64(t[k][b:b + 1]) for k in ("q_nope", "q_pe", "kv_cache", "pe_cache", "topk_idx",
+                                                     "end_pos")}
+        t0 = time.perf_counter()
+        O.decode_step(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], wkv, x["topk_idx"], x["end_pos"],
+                      inv, scale)
+        spent += time.perf_counter() - t0
+        done += 1
+    return done, spent
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args):
+    from sparse_latent_attention_decode_b300 import mla, synth
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+
+    wl = synth.workload(args.workload, seed=replica_seed(rank, args.seed))
+    t = synth.make_inputs(wl, seed=replica_seed(rank, args.seed))
+    d = {k: v.to(dev) for k, v in t.items()}
+    B, K = wl.B, wl.row_stride()
+    rows = selected_rows(d["topk_idx"], d["end_pos"])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    step = mla.DecodeStep(B, K, device=dev)
+    args_dev = (d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+
+    # ---- device-resident inputs
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step(*args_dev)
+    torch.cuda.synchronize()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    kt = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    with mla.ProfileHook() as hook:
+        for i in range(args.steps):
+            flush.fill_((i + 7) & 0xFF)
+            hook.set_events(kt[2 * i], kt[2 * i + 1])
+            st[2 * i].record()
+            step(*args_dev)
+            st[2 * i + 1].record()
+        launches = hook.launches
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step.check_status()
+    step_ms = [st[2 * i].elapsed_time(st[2 * i + 1]) for i in range(args.steps)]
+    kern_ms = [kt[2 * i].elapsed_time(kt[2 * i + 1]) for i in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world, dev)
+    kern = statistics.mean(kern_ms)
+
+    # ---- end to end through the host-buffer API
+    h = {k: t[k].pin_memory() for k in ("q_nope", "q_pe", "topk_idx", "end_pos")}
+    hstep = mla.HostDecodeStep(B, K, device=dev)
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        hstep.run(h["q_nope"], h["q_pe"], h["topk_idx"], h["end_pos"], d["kv_cache"], d["pe_cache"], d["wkv_b"])
+    torch.cuda.synchronize()
+    et = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_((i + 3) & 0xFF)
+        et[2 * i].record()
+        hstep.run(h["q_nope"], h["q_pe"], h["topk_idx"], h["end_pos"], d["kv_cache"], d["pe_cache"], d["wkv_b"])
+        et[2 * i + 1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(statistics.mean(et[2 * i].elapsed_time(et[2 * i + 1]) for i in range(args.steps)),
+                            world, dev)
+
+    if rank != 0:
+        return None
+
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm else "fallback"
+    hbm = float(hbm) if hbm else FALLBACK_HBM_GBS
+    alg_bytes = rows * ROW_BYTES
+    achieved = alg_bytes / (kern * 1e-3) / 1e9
+    kernel_src = os.path.join(ROOT, "sparse_latent_attention_decode_b300", "csrc", "decode.cu")
+    traffic = traffic_record(kernel_src)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n, secs = oracle_sample(t, wl, budget_s=args.cpu_budget)
+        cpu = {"value": n / secs, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"sequences 0..{n - 1} of the {args.workload} batch ({n} of {B}); float64 numpy, "
+                         f"full step per sequence (RoPE, absorb, masked scores over all end_pos keys, softmax, "
+                         f"PV, up-projection); {secs:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": world * B / (ms_max * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch_per_gpu": B, "global_batch": world * B,
+                   "end_pos": (wl.end_pos[0] if len(set(wl.end_pos)) == 1 else
+                               f"{min(wl.end_pos)}..{max(wl.end_pos)}"),
+                   "topk_row": K, "selected_rows_per_gpu": rows, "S_cap": wl.S_cap, "heads": 128,
+                   "kv_lora": 512, "rope_dim": 64, "l2": "flushed by a 256 MiB write before each step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": hstep.h2d_bytes(), "d2h_bytes_per_step": hstep.d2h_bytes()},
+        "roofline": {"bound": "hbm", "kernel": "mla_sparse_decode attention kernel",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
+                     "alg_bytes_per_launch": alg_bytes, "kernel_ms": kern},
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "gpu_launches": launches,
+        "wall_s_timed_region": wall,
+    }
+    return line
+
+
+# ----------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    from sparse_latent_attention_decode_b300 import synth
+    wl = synth.workload(args.workload, seed=replica_seed(0, args.seed))
+    t = synth.make_inputs(wl, seed=replica_seed(0, args.seed))
+    n_total = args.warmup + args.steps
+    times = []
+    for i in range(n_total):
+        sub = {k: (v[i % wl.B:i % wl.B + 1] if k != "wkv_b" else v) for k, v in t.items()}
+        sub_wl = synth.Workload(wl.name, 1, [wl.end_pos[i % wl.B]], wl.selection, wl.k, wl.K, wl.S_cap)
+        _, secs = oracle_sample(sub, sub_wl, budget_s=0.0, max_seqs=1)
+        if i >= args.warmup:
+            times.append(secs)
+    sec = statistics.mean(times)
+    v = 1.0 / sec
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch_per_step": 1, "S_cap": wl.S_cap,
+                       "note": "float64 CPU oracle, one sequence of the batch per step"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                             "sample": f"one sequence of {args.workload} per step, {args.steps} steps"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

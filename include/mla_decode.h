@@ -1,0 +1,189 @@
+/*
+ * mla_decode.h -- C ABI of the B300 (sm_103a) library for one decode step of
+ * absorbed, top-k-sparse latent attention (DeepSeek-V3.2-Exp sparse MLA).
+ *
+ * The step, as the DeepSeek-V3.2-Exp atlas pages state it ("Rotated query
+ * part" / "Query content heads" / "Attention weights", excerpt mla-decode):
+ *
+ *   q~[b,h,:]   = q_nope[b,h,:] . W_UK[h]                     (key absorption)
+ *   s[b,h,t]    = (q~[b,h,:] . kv[b,t,:] + rope(q_pe)[b,h,:] . pe[b,t,:]) * scale
+ *   s[b,h,t]   += 0 for t in topk_idx[b,:], -inf otherwise     (selection mask)
+ *   p           = softmax_t(s)
+ *   o[b,h,:]    = sum_t p[b,h,t] kv[b,t,:]
+ *   out[b,h,:]  = W_UV[h] . o[b,h,:]                          (value up-projection)
+ *
+ * with wkv_b [128*256, 512] viewed [128, 256, 512]: rows 0..127 of head h are
+ * W_UK[h] (128 x 512), rows 128..255 are W_UV[h] (128 x 512).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - H = 128 heads, d_nope = 128, d_rope = 64, d_v = 128, kv_lora = 512 are
+ *    fixed (the kernels are specialised for them).
+ *  - mla_bf16 is the raw bit pattern of an IEEE bfloat16.
+ *  - Every tensor pointer is a DEVICE pointer (cudaMalloc / torch CUDA memory)
+ *    unless stated otherwise, row-major and contiguous, 16-byte aligned.
+ *  - The caller owns every buffer (inputs, outputs, workspace, status word).
+ *    The library allocates nothing and keeps no state between calls, except
+ *    cached per-device properties read on first use.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  A call returns after enqueueing its kernels.
+ *  - Return value: MLA_OK (0) on success; a negative MLA_ERR_* code when an
+ *    argument check fails on the host (nothing is enqueued then), or
+ *    MLA_ERR_CUDA when a launch fails.  No exception crosses the ABI.
+ *  - Conditions only the device can see (an end_pos outside [1, S_cap], a
+ *    position outside the rotary table, a bounded wait that ran out) are OR-ed
+ *    as MLA_DEV_* bits into *dev_status (when dev_status is non-NULL); read it
+ *    after synchronising the stream.  Affected sequences produce zeros.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mla_bf16;
+typedef struct CUstream_st *mla_stream_t; /* same type as cudaStream_t */
+
+#define MLA_N_HEADS 128
+#define MLA_D_NOPE 128
+#define MLA_D_ROPE 64
+#define MLA_D_V 128
+#define MLA_KV_LORA 512
+#define MLA_Q_LAT 576 /* kv_lora + d_rope */
+
+/* host-side return codes */
+#define MLA_OK 0
+#define MLA_ERR_NULL (-1)        /* a required pointer is NULL */
+#define MLA_ERR_ALIGN (-2)       /* a pointer is not 16-byte aligned */
+#define MLA_ERR_SIZE (-3)        /* a size argument is out of range */
+#define MLA_ERR_WORKSPACE (-4)   /* workspace smaller than required */
+#define MLA_ERR_CUDA (-5)        /* a CUDA launch or query failed */
+#define MLA_ERR_DEVICE (-6)      /* current device is not sm_103 */
+
+/* device-side status bits (OR-ed into *dev_status) */
+#define MLA_DEV_BAD_END_POS 1    /* end_pos[b] < 1 or > S_cap: sequence b skipped */
+#define MLA_DEV_BAD_POSITION 2   /* end_pos[b]-1 outside the rotary table */
+#define MLA_DEV_TIMEOUT 4        /* a bounded on-chip wait gave up */
+
+/* Rotary / YaRN parameters.  Defaults (mla_rope_params_default) are those of
+ * the "Transformer blocks" page, excerpt model-args: max_seq_len 16384,
+ * original_seq_len 4096, rope_theta 1e4, rope_factor 40, beta_fast 32,
+ * beta_slow 1, mscale 1, rope_dim 64. */
+typedef struct mla_rope_params {
+    int32_t rope_dim;         /* must be 64 */
+    int32_t max_seq_len;      /* rows of the rotary table */
+    int32_t original_seq_len; /* YaRN is applied when max_seq_len > this */
+    int32_t reserved;         /* set to 0 */
+    double rope_theta;
+    double rope_factor;
+    double beta_fast;
+    double beta_slow;
+    double mscale;
+} mla_rope_params;
+
+/* Fill *p with the defaults above (host only). */
+void mla_rope_params_default(mla_rope_params *p);
+
+/* Softmax scale of the step ("Query heads" page, excerpt mla-init):
+ * qk_head_dim^-0.5, times (0.1*mscale*ln(rope_factor) + 1)^2 when
+ * max_seq_len > original_seq_len.  Host-only helper; qk_head_dim = 192 for
+ * this block.  Returns a negative value when p is NULL or qk_head_dim <= 0. */
+double mla_softmax_scale(const mla_rope_params *p, int qk_head_dim);
+
+/* rope_freqs_init -- the rotary coefficient table ("Transformer blocks" page,
+ * RoPE coefficients panel, excerpt rope).
+ *   cis  [max_seq_len][32][2] fp32, device, written: (cos, sin) of t * f'_i,
+ *        f'_i = YaRN-blended 1 / theta^(2i/64).  Angles and sincos are
+ *        evaluated in fp64 on the device and stored rounded to fp32.
+ *   p    host pointer to the parameters (copied by value at the call).
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (rope_dim != 64,
+ * max_seq_len < 1 or > 1<<24, theta/factor <= 0, beta_fast <= 0 or
+ * beta_slow <= 0). */
+int rope_freqs_init(float *cis, const mla_rope_params *p, mla_stream_t stream);
+
+/* mla_rope_apply -- interleaved rotary embedding of the query's rotary part
+ * ("Rotated query part" page, excerpt apply-rope): each pair
+ * (x[2i], x[2i+1]) is multiplied, as a complex number, by cis[pos_b][i] in
+ * fp32, with pos_b = end_pos[b] - 1.
+ *   q_pe      [B][128][64] bf16, device
+ *   cis       [max_seq_len][32][2] fp32 from rope_freqs_init
+ *   end_pos   [B] int32, device
+ *   q_pe_rot  [B][128][64] fp32, device, written (zeros for a sequence whose
+ *             position is outside [0, max_seq_len): MLA_DEV_BAD_POSITION)
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 65535,
+ * max_seq_len < 1). */
+int mla_rope_apply(const mla_bf16 *q_pe, const float *cis, int max_seq_len, const int32_t *end_pos,
+                   int B, float *q_pe_rot, int32_t *dev_status, mla_stream_t stream);
+
+/* mla_absorb_q -- the query of the latent attention: key absorption
+ * ("Query content heads" page, excerpt mla-decode, first einsum) with the
+ * RoPE of q_pe fused in:
+ *   q_lat[b,h,0:512]   = bf16( sum_d q_nope[b,h,d] * W_UK[h][d][:] )  (fp32 accumulate)
+ *   q_lat[b,h,512:576] = bf16( rope(q_pe[b,h,:], pos_b) )
+ *   q_nope [B][128][128] bf16, q_pe [B][128][64] bf16, cis as above,
+ *   end_pos [B] int32, wkv_b [32768][512] bf16, q_lat [B][128][576] bf16 (written).
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096). */
+int mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const float *cis, int max_seq_len,
+                 const int32_t *end_pos, const mla_bf16 *wkv_b, int B, mla_bf16 *q_lat,
+                 int32_t *dev_status, mla_stream_t stream);
+
+/* Bytes of device workspace mla_sparse_decode needs for B sequences whose
+ * selection rows hold K entries.  0 when B or K is out of range. */
+size_t mla_sparse_decode_workspace_size(int B, int K);
+
+/* mla_sparse_decode -- scores of every head against the selected rows of the
+ * shared 576-wide cache, softmax over the selected set, probability-weighted
+ * sum of the latent rows, and (when wkv_b is given) the value up-projection
+ * ("Attention weights" page, excerpt mla-decode, scores .. last einsum).
+ *   q_lat     [B][128][576] bf16 (from mla_absorb_q)
+ *   kv_cache  [B][S_cap][512] bf16, pe_cache [B][S_cap][64] bf16
+ *   topk_idx  [B][K] int32: positions selected for sequence b.  Entries < 0
+ *             or >= end_pos[b] are padding and ignored.  Valid entries of a
+ *             row must be distinct (the selection is a set; a repeated
+ *             position would be counted twice).
+ *   end_pos   [B] int32: cached keys of sequence b (1 <= end_pos <= S_cap)
+ *   softmax_scale: multiplies the raw scores (see mla_softmax_scale)
+ *   wkv_b     NULL, or [32768][512] bf16 for the fused up-projection
+ *   out       wkv_b != NULL: [B][128][128] fp32 head outputs;
+ *             wkv_b == NULL: [B][128][512] fp32 normalised latent outputs o.
+ *             A sequence with no valid selected position yields zeros.
+ *   workspace device scratch of at least mla_sparse_decode_workspace_size(B, K)
+ *             bytes, 256-byte aligned; contents on entry do not matter.
+ *   dev_status optional device int32, MLA_DEV_* bits OR-ed in.
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096,
+ * K < 1 or > 1<<20, S_cap < 1), MLA_ERR_WORKSPACE. */
+int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla_bf16 *pe_cache,
+                      int S_cap, const int32_t *topk_idx, int K, const int32_t *end_pos, int B,
+                      float softmax_scale, const mla_bf16 *wkv_b, float *out, void *workspace,
+                      size_t ws_bytes, int32_t *dev_status, mla_stream_t stream);
+
+/* mla_out_up -- value up-projection alone ("Attention weights" page, excerpt
+ * mla-decode, last einsum): out[b,h,d] = sum_c o_lat[b,h,c] * W_UV[h][d][c],
+ * with o_lat rounded to bf16 and fp32 accumulation.
+ *   o_lat [B][128][512] fp32, wkv_b [32768][512] bf16, out [B][128][128] fp32.
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096). */
+int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, float *out, mla_stream_t stream);
+
+/* Profiling hook for the calling host thread (the library's only mutable
+ * state, and it is per thread).  While set:
+ *   - every entry point adds the number of kernels it enqueues to
+ *     *launch_count (when launch_count is non-NULL);
+ *   - mla_sparse_decode records ev_start (a cudaEvent_t) on its stream just
+ *     before its attention kernel and ev_stop just after it (when both are
+ *     non-NULL), so the attention kernel alone can be timed.
+ * Pass NULL for all three to clear.  Returns MLA_OK. */
+int mla_profile_hook(void *ev_start, void *ev_stop, int64_t *launch_count);
+
+/* Static description of a return code or of a set of MLA_DEV_* bits
+ * (pass the negative return code, or the status word as a positive value). */
+const char *mla_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

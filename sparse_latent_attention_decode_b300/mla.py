@@ -1,0 +1,284 @@
+"""Thin ctypes binding over the C ABI of ``libmla_decode.so`` (include/mla_decode.h).
+
+Argument marshalling only: every step of the decode runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the
+library has not been built, importing this module raises; there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla_decode.so")
+
+N_HEADS, D_NOPE, D_ROPE, D_V, KV_LORA, Q_LAT = 128, 128, 64, 128, 512, 576
+QK_HEAD_DIM = D_NOPE + D_ROPE
+
+MLA_OK = 0
+MLA_DEV_BAD_END_POS = 1
+MLA_DEV_BAD_POSITION = 2
+MLA_DEV_TIMEOUT = 4
+
+
+class MLAError(RuntimeError):
+    """A library call returned a non-zero status."""
+
+
+class RopeParams(ctypes.Structure):
+    _fields_ = [("rope_dim", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("original_seq_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double), ("rope_factor", ctypes.c_double),
+                ("beta_fast", ctypes.c_double), ("beta_slow", ctypes.c_double),
+                ("mscale", ctypes.c_double)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m sparse_latent_attention_decode_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, Z, F, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_double
+    sig = {
+        "mla_rope_params_default": (None, [ctypes.POINTER(RopeParams)]),
+        "mla_softmax_scale": (D, [ctypes.POINTER(RopeParams), I]),
+        "rope_freqs_init": (I, [P, ctypes.POINTER(RopeParams), P]),
+        "mla_rope_apply": (I, [P, P, I, P, I, P, P, P]),
+        "mla_absorb_q": (I, [P, P, P, I, P, P, I, P, P, P]),
+        "mla_sparse_decode_workspace_size": (Z, [I, I]),
+        "mla_sparse_decode": (I, [P, P, P, I, P, I, P, I, F, P, P, P, Z, P, P]),
+        "mla_out_up": (I, [P, P, I, P, P]),
+        "mla_status_string": (ctypes.c_char_p, [I]),
+        "mla_profile_hook": (I, [P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply",
+            "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
+            "mla_status_string", "mla_profile_hook")
+
+
+def status_string(code: int) -> str:
+    return _lib.mla_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != MLA_OK:
+        raise MLAError(f"{what}: {status_string(code)} (code {code})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def rope_params(max_seq_len: int = 16384, original_seq_len: int = 4096, rope_theta: float = 10000.0,
+                rope_factor: float = 40.0, beta_fast: float = 32.0, beta_slow: float = 1.0,
+                mscale: float = 1.0) -> RopeParams:
+    p = RopeParams()
+    _lib.mla_rope_params_default(ctypes.byref(p))
+    p.max_seq_len, p.original_seq_len = max_seq_len, original_seq_len
+    p.rope_theta, p.rope_factor = rope_theta, rope_factor
+    p.beta_fast, p.beta_slow, p.mscale = beta_fast, beta_slow, mscale
+    return p
+
+
+def softmax_scale(params: RopeParams | None = None, qk_head_dim: int = QK_HEAD_DIM) -> float:
+    p = params if params is not None else rope_params()
+    return float(_lib.mla_softmax_scale(ctypes.byref(p), qk_head_dim))
+
+
+def rope_freqs_init(params: RopeParams | None = None, device="cuda", out=None) -> torch.Tensor:
+    """Rotary table [max_seq_len, 32, 2] fp32 of (cos, sin)."""
+    p = params if params is not None else rope_params()
+    if out is None:
+        out = torch.empty(p.max_seq_len, D_ROPE // 2, 2, dtype=torch.float32, device=device)
+    _need(out, "cis", torch.float32, (p.max_seq_len, D_ROPE // 2, 2))
+    _check(_lib.rope_freqs_init(_ptr(out), ctypes.byref(p), _stream(out.device)), "rope_freqs_init")
+    return out
+
+
+def mla_rope_apply(q_pe, cis, end_pos, out=None, dev_status=None) -> torch.Tensor:
+    B = q_pe.shape[0]
+    _need(q_pe, "q_pe", torch.bfloat16, (B, N_HEADS, D_ROPE))
+    _need(cis, "cis", torch.float32)
+    _need(end_pos, "end_pos", torch.int32, (B,))
+    if out is None:
+        out = torch.empty(B, N_HEADS, D_ROPE, dtype=torch.float32, device=q_pe.device)
+    _need(out, "q_pe_rot", torch.float32, (B, N_HEADS, D_ROPE))
+    _check(_lib.mla_rope_apply(_ptr(q_pe), _ptr(cis), cis.shape[0], _ptr(end_pos), B, _ptr(out),
+                               _ptr(dev_status), _stream(q_pe.device)), "mla_rope_apply")
+    return out
+
+
+def mla_absorb_q(q_nope, q_pe, cis, end_pos, wkv_b, out=None, dev_status=None) -> torch.Tensor:
+    B = q_nope.shape[0]
+    _need(q_nope, "q_nope", torch.bfloat16, (B, N_HEADS, D_NOPE))
+    _need(q_pe, "q_pe", torch.bfloat16, (B, N_HEADS, D_ROPE))
+    _need(cis, "cis", torch.float32)
+    _need(end_pos, "end_pos", torch.int32, (B,))
+    _need(wkv_b, "wkv_b", torch.bfloat16, (N_HEADS * (D_NOPE + D_V), KV_LORA))
+    if out is None:
+        out = torch.empty(B, N_HEADS, Q_LAT, dtype=torch.bfloat16, device=q_nope.device)
+    _need(out, "q_lat", torch.bfloat16, (B, N_HEADS, Q_LAT))
+    _check(_lib.mla_absorb_q(_ptr(q_nope), _ptr(q_pe), _ptr(cis), cis.shape[0], _ptr(end_pos), _ptr(wkv_b), B,
+                             _ptr(out), _ptr(dev_status), _stream(q_nope.device)), "mla_absorb_q")
+    return out
+
+
+def workspace_size(B: int, K: int) -> int:
+    n = int(_lib.mla_sparse_decode_workspace_size(B, K))
+    if n == 0:
+        raise MLAError(f"workspace size undefined for B={B}, K={K}")
+    return n
+
+
+def mla_sparse_decode(q_lat, kv_cache, pe_cache, topk_idx, end_pos, softmax_scale, wkv_b=None, out=None,
+                      workspace=None, dev_status=None) -> torch.Tensor:
+    """Latent attention over the selected rows; with wkv_b the result is the
+    head output [B,128,128], without it the normalised latent o [B,128,512]."""
+    B, K = topk_idx.shape
+    S_cap = kv_cache.shape[1]
+    _need(q_lat, "q_lat", torch.bfloat16, (B, N_HEADS, Q_LAT))
+    _need(kv_cache, "kv_cache", torch.bfloat16, (B, S_cap, KV_LORA))
+    _need(pe_cache, "pe_cache", torch.bfloat16, (B, S_cap, D_ROPE))
+    _need(topk_idx, "topk_idx", torch.int32, (B, K))
+    _need(end_pos, "end_pos", torch.int32, (B,))
+    if wkv_b is not None:
+        _need(wkv_b, "wkv_b", torch.bfloat16, (N_HEADS * (D_NOPE + D_V), KV_LORA))
+    width = D_V if wkv_b is not None else KV_LORA
+    if out is None:
+        out = torch.empty(B, N_HEADS, width, dtype=torch.float32, device=q_lat.device)
+    _need(out, "out", torch.float32, (B, N_HEADS, width))
+    if workspace is None:
+        workspace = torch.empty(workspace_size(B, K), dtype=torch.uint8, device=q_lat.device)
+    _check(_lib.mla_sparse_decode(_ptr(q_lat), _ptr(kv_cache), _ptr(pe_cache), S_cap, _ptr(topk_idx), K,
+                                  _ptr(end_pos), B, float(softmax_scale), _ptr(wkv_b), _ptr(out),
+                                  _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                  _stream(q_lat.device)), "mla_sparse_decode")
+    return out
+
+
+def mla_out_up(o_lat, wkv_b, out=None) -> torch.Tensor:
+    B = o_lat.shape[0]
+    _need(o_lat, "o_lat", torch.float32, (B, N_HEADS, KV_LORA))
+    _need(wkv_b, "wkv_b", torch.bfloat16, (N_HEADS * (D_NOPE + D_V), KV_LORA))
+    if out is None:
+        out = torch.empty(B, N_HEADS, D_V, dtype=torch.float32, device=o_lat.device)
+    _need(out, "out", torch.float32, (B, N_HEADS, D_V))
+    _check(_lib.mla_out_up(_ptr(o_lat), _ptr(wkv_b), B, _ptr(out), _stream(o_lat.device)), "mla_out_up")
+    return out
+
+
+class ProfileHook:
+    """Context manager around the library's per-thread profiling hook: counts
+    the kernels the library enqueues and (optionally) records a pair of CUDA
+    events around the attention kernel of each mla_sparse_decode call."""
+
+    def __init__(self, ev_start=None, ev_stop=None):
+        self.count = ctypes.c_int64(0)
+        self.ev_start, self.ev_stop = ev_start, ev_stop
+
+    def set_events(self, ev_start, ev_stop):
+        self.ev_start, self.ev_stop = ev_start, ev_stop
+        self._arm()
+
+    def _arm(self):
+        s = ctypes.c_void_p(self.ev_start.cuda_event) if self.ev_start is not None else None
+        e = ctypes.c_void_p(self.ev_stop.cuda_event) if self.ev_stop is not None else None
+        _lib.mla_profile_hook(s, e, ctypes.byref(self.count))
+
+    def __enter__(self):
+        self._arm()
+        return self
+
+    def __exit__(self, *exc):
+        _lib.mla_profile_hook(None, None, None)
+        return False
+
+    @property
+    def launches(self) -> int:
+        return int(self.count.value)
+
+
+class DecodeStep:
+    """One decode step with its buffers held: absorb (RoPE fused) -> sparse
+    attention -> value up-projection, three library calls on the current
+    stream.  The caches and wkv_b are resident device state; the per-step
+    inputs are the query parts, the selection and end_pos."""
+
+    def __init__(self, B: int, K: int, device="cuda", params: RopeParams | None = None):
+        self.B, self.K, self.device = B, K, torch.device(device)
+        self.params = params if params is not None else rope_params()
+        self.scale = softmax_scale(self.params)
+        self.cis = rope_freqs_init(self.params, device=self.device)
+        self.q_lat = torch.empty(B, N_HEADS, Q_LAT, dtype=torch.bfloat16, device=self.device)
+        self.out = torch.empty(B, N_HEADS, D_V, dtype=torch.float32, device=self.device)
+        self.workspace = torch.empty(workspace_size(B, K), dtype=torch.uint8, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def __call__(self, q_nope, q_pe, kv_cache, pe_cache, wkv_b, topk_idx, end_pos):
+        mla_absorb_q(q_nope, q_pe, self.cis, end_pos, wkv_b, out=self.q_lat, dev_status=self.status)
+        return mla_sparse_decode(self.q_lat, kv_cache, pe_cache, topk_idx, end_pos, self.scale, wkv_b=wkv_b,
+                                 out=self.out, workspace=self.workspace, dev_status=self.status)
+
+    def check_status(self):
+        v = int(self.status.item())
+        if v:
+            raise MLAError(f"device status: {status_string(v)} (bits {v})")
+
+
+class HostDecodeStep(DecodeStep):
+    """End-to-end step from host buffers: per-step inputs are copied from
+    pinned host memory to the device, the three library calls run, and the
+    head outputs are copied back into a pinned host buffer."""
+
+    def __init__(self, B: int, K: int, device="cuda", params: RopeParams | None = None):
+        super().__init__(B, K, device, params)
+        dev = self.device
+        self.d_q_nope = torch.empty(B, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=dev)
+        self.d_q_pe = torch.empty(B, N_HEADS, D_ROPE, dtype=torch.bfloat16, device=dev)
+        self.d_topk = torch.empty(B, K, dtype=torch.int32, device=dev)
+        self.d_end = torch.empty(B, dtype=torch.int32, device=dev)
+        self.h_out = torch.empty(B, N_HEADS, D_V, dtype=torch.float32).pin_memory()
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.d_q_nope, self.d_q_pe, self.d_topk, self.d_end))
+
+    def d2h_bytes(self):
+        return self.h_out.numel() * self.h_out.element_size()
+
+    def run(self, h_q_nope, h_q_pe, h_topk, h_end, kv_cache, pe_cache, wkv_b):
+        self.d_q_nope.copy_(h_q_nope, non_blocking=True)
+        self.d_q_pe.copy_(h_q_pe, non_blocking=True)
+        self.d_topk.copy_(h_topk, non_blocking=True)
+        self.d_end.copy_(h_end, non_blocking=True)
+        out = self(self.d_q_nope, self.d_q_pe, kv_cache, pe_cache, wkv_b, self.d_topk, self.d_end)
+        self.h_out.copy_(out, non_blocking=True)
+        return self.h_out

@@ -1,0 +1,113 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_latent_attention_decode_b300 import mla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for want in ("rope_freqs_init", "mla_rope_apply", "mla_absorb_q", "mla_sparse_decode", "mla_out_up",
+                 "mla_sparse_decode_workspace_size", "mla_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(mla.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(mla.EXPORTED) <= set(_declared_functions())
+
+
+def test_softmax_scale_from_the_library_matches_closed_form():
+    g = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "softmax_scale_closed_form.txt")):
+        if line.strip() and not line.startswith("#"):
+            k, v = line.split()
+            g[k] = float(v)
+    assert mla.softmax_scale() == pytest.approx(g["softmax_scale"], rel=1e-15)
+    p = mla.rope_params(max_seq_len=4096)
+    assert mla.softmax_scale(p) == pytest.approx(g["softmax_scale_no_yarn"], rel=1e-15)
+
+
+def test_workspace_size_is_monotone_and_rejects_bad_sizes():
+    lib = mla._lib
+    assert lib.mla_sparse_decode_workspace_size(0, 2048) == 0
+    assert lib.mla_sparse_decode_workspace_size(64, 0) == 0
+    assert lib.mla_sparse_decode_workspace_size(5000, 16) == 0
+    a = lib.mla_sparse_decode_workspace_size(1, 2048)
+    b = lib.mla_sparse_decode_workspace_size(64, 2048)
+    c = lib.mla_sparse_decode_workspace_size(64, 16384)
+    assert 0 < a < b <= c
+    assert b % 256 == 0
+
+
+P = ctypes.c_void_p
+GOOD = P(0x10000)       # never dereferenced: every call below fails its host check first
+MISALIGNED = P(0x10004)
+
+
+def test_host_argument_checks_return_codes_without_launching():
+    lib = mla._lib
+    nul = None
+    # NULL pointers
+    assert lib.mla_sparse_decode(nul, GOOD, GOOD, 16, GOOD, 8, GOOD, 1, 1.0, nul, GOOD, GOOD, 1 << 30, nul,
+                                 nul) == -1
+    assert lib.mla_absorb_q(GOOD, nul, GOOD, 16, GOOD, GOOD, 1, GOOD, nul, nul) == -1
+    assert lib.mla_out_up(GOOD, nul, 1, GOOD, nul) == -1
+    assert lib.mla_rope_apply(GOOD, GOOD, 16, nul, 1, GOOD, nul, nul) == -1
+    assert lib.rope_freqs_init(nul, ctypes.byref(mla.rope_params()), nul) == -1
+    # alignment
+    assert lib.mla_out_up(MISALIGNED, GOOD, 1, GOOD, nul) == -2
+    assert lib.mla_sparse_decode(GOOD, GOOD, GOOD, 16, GOOD, 8, GOOD, 1, 1.0, nul, GOOD, P(0x10010), 1 << 30,
+                                 nul, nul) == -2          # workspace must be 256-byte aligned
+    # sizes
+    assert lib.mla_sparse_decode(GOOD, GOOD, GOOD, 16, GOOD, 8, GOOD, 0, 1.0, nul, GOOD, GOOD, 1 << 30, nul,
+                                 nul) == -3
+    assert lib.mla_sparse_decode(GOOD, GOOD, GOOD, 0, GOOD, 8, GOOD, 1, 1.0, nul, GOOD, GOOD, 1 << 30, nul,
+                                 nul) == -3
+    assert lib.mla_sparse_decode(GOOD, GOOD, GOOD, 16, GOOD, 0, GOOD, 1, 1.0, nul, GOOD, GOOD, 1 << 30, nul,
+                                 nul) == -3
+    assert lib.mla_absorb_q(GOOD, GOOD, GOOD, 16, GOOD, GOOD, 4097, GOOD, nul, nul) == -3
+    assert lib.mla_out_up(GOOD, GOOD, 0, GOOD, nul) == -3
+    bad = mla.rope_params()
+    bad.rope_dim = 32
+    assert lib.rope_freqs_init(GOOD, ctypes.byref(bad), nul) == -3
+    bad = mla.rope_params()
+    bad.rope_factor = 0.0
+    assert lib.rope_freqs_init(GOOD, ctypes.byref(bad), nul) == -3
+    # workspace too small
+    need = lib.mla_sparse_decode_workspace_size(2, 64)
+    assert lib.mla_sparse_decode(GOOD, GOOD, GOOD, 16, GOOD, 64, GOOD, 2, 1.0, nul, GOOD, GOOD, need - 1, nul,
+                                 nul) == -4
+
+
+def test_status_strings():
+    assert mla.status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5, -6):
+        assert mla.status_string(code) not in ("ok", "unknown status code")
+    assert "end_pos" in mla.status_string(1)
+    assert "timed out" in mla.status_string(4)
+    assert mla.status_string(-99) == "unknown status code"
+
+
+def test_python_wrappers_reject_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mla.mla_rope_apply(x, torch.zeros(16, 32, 2), torch.ones(1, dtype=torch.int32))

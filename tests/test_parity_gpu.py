@@ -1,0 +1,226 @@
+"""GPU parity: every entry point of the C ABI against the float64 oracle on
+identical seeded inputs.  Needs a B300 (sm_103a)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mla_oracle as O
+from sparse_latent_attention_decode_b300 import synth
+from tests import parity_util as U
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from sparse_latent_attention_decode_b300 import mla
+
+
+def _dev(t):
+    return {k: v.cuda() for k, v in t.items()}
+
+
+class _PerSeq:
+    """Widen one sequence of a large host tensor to float64 on demand."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, b):
+        return synth.to_f64(self.t[b])
+
+
+def _oracle_view(t):
+    x = {k: synth.to_f64(v) for k, v in t.items() if k not in ("kv_cache", "pe_cache")}
+    x["kv_cache"] = _PerSeq(t["kv_cache"])
+    x["pe_cache"] = _PerSeq(t["pe_cache"])
+    return x
+
+
+# ----------------------------------------------------------------- RoPE
+def test_rope_table_matches_oracle():
+    cis = mla.rope_freqs_init().cpu().double().numpy()
+    ora = O.freqs_cis(np.arange(16384), U.INV_FREQ)
+    assert np.abs(cis[..., 0] - ora.real).max() <= 2e-7
+    assert np.abs(cis[..., 1] - ora.imag).max() <= 2e-7
+
+
+def test_rope_table_without_yarn_and_short_table():
+    p = mla.rope_params(max_seq_len=4096)
+    cis = mla.rope_freqs_init(p).cpu().double().numpy()
+    ora = O.freqs_cis(np.arange(4096), O.yarn_inv_freq(max_seq_len=4096))
+    assert np.abs(cis[..., 0] - ora.real).max() <= 2e-7
+    assert np.abs(cis[..., 1] - ora.imag).max() <= 2e-7
+
+
+def test_rope_apply_matches_oracle():
+    g = torch.Generator().manual_seed(7)
+    end = torch.tensor([1, 2, 1001, 4096, 8191, 16384], dtype=torch.int32)
+    q_pe = torch.randn(6, 128, 64, generator=g).to(torch.bfloat16)
+    cis = mla.rope_freqs_init()
+    got = mla.mla_rope_apply(q_pe.cuda(), cis, end.cuda()).cpu().double().numpy()
+    x = synth.to_f64(q_pe)
+    ora = O.rope_for_batch(x, end.numpy(), U.INV_FREQ)
+    U.assert_rope_close(got, ora, x, "rope")
+
+
+def test_rope_apply_reports_bad_position():
+    cis = mla.rope_freqs_init()
+    q_pe = torch.ones(2, 128, 64, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mla.mla_rope_apply(q_pe, cis, torch.tensor([0, 16385], dtype=torch.int32, device="cuda"), dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & mla.MLA_DEV_BAD_POSITION
+    assert torch.all(out == 0)
+
+
+# ----------------------------------------------------------------- absorb / up-projection
+@pytest.mark.parametrize("B", [1, 3, 64, 130])
+def test_absorb_matches_oracle(B):
+    t = synth.make_inputs(synth.small_workload(B, [8] * B, k=1, K=1, S_cap=8), seed=11)
+    # positions spread over the whole rotary table
+    t["end_pos"] = torch.tensor([1 + (977 * b) % 16384 for b in range(B)], dtype=torch.int32)
+    d = _dev(t)
+    cis = mla.rope_freqs_init()
+    q_lat = mla.mla_absorb_q(d["q_nope"], d["q_pe"], cis, d["end_pos"], d["wkv_b"]).cpu()
+    x = U.oracle_inputs(t)
+    ora = U.oracle_q_lat(x, list(range(B)))
+    got = synth.to_f64(q_lat)
+    U.assert_attn_close(got[..., :512], ora[..., :512], "absorbed q")
+    U.assert_attn_close(got[..., 512:], ora[..., 512:], "rotated q_pe")
+    # each element is the bf16 rounding of an fp32 sum: within 2^-8 relative
+    assert np.all(np.abs(got - ora) <= 2.0 ** -8 * np.abs(ora) + 1e-6 * np.abs(ora).max())
+
+
+@pytest.mark.parametrize("B", [1, 5, 64])
+def test_out_up_matches_oracle(B):
+    g = torch.Generator().manual_seed(13)
+    o = torch.randn(B, 128, 512, generator=g)
+    t = synth.make_inputs(synth.small_workload(1, [4], k=1, K=1, S_cap=4), seed=2)
+    got = mla.mla_out_up(o.cuda(), t["wkv_b"].cuda()).cpu().double().numpy()
+    ora = O.out_up(o.double().numpy(), synth.to_f64(t["wkv_b"]))
+    U.assert_attn_close(got, ora, "out_up")
+
+
+# ----------------------------------------------------------------- attention, small cases
+SMALL = [
+    # (B, end_pos, k, K, S_cap, selection)
+    (1, [8], 8, 8, 8, "uniform"),
+    (3, [600, 333, 37], 300, 300, 600, "uniform"),          # ragged tail: K not a multiple of 32
+    (2, [1000, 1000], 1000, 1000, 1024, "all"),
+    (4, [2100, 1500, 2048, 700], 1100, 1100, 2112, "recent_half"),
+    (2, [5000, 4097], 2048, 2048, 5000, "uniform"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"B{c[0]}_K{c[3]}" for c in SMALL])
+def test_sparse_decode_small_matches_oracle(case):
+    B, ep, k, K, S, sel = case
+    t = synth.make_inputs(synth.small_workload(B, ep, k=k, K=K, S_cap=S, selection=sel), seed=3)
+    d = _dev(t)
+    x = U.oracle_inputs(t)
+    step = mla.DecodeStep(B, K)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    step.check_status()
+    U.assert_attn_close(out.cpu().numpy(), U.oracle_out(x, list(range(B))), "head outputs")
+    # the attention stage alone, with the GPU's own bf16 query
+    o = mla.mla_sparse_decode(step.q_lat, d["kv_cache"], d["pe_cache"], d["topk_idx"], d["end_pos"], step.scale)
+    q_gpu = synth.to_f64(step.q_lat.cpu())
+    U.assert_attn_close(o.cpu().numpy(), U.oracle_o_lat(x, list(range(B)), q_lat=q_gpu), "latent o")
+
+
+def test_padding_out_of_range_and_empty_rows():
+    B, S = 3, 512
+    t = synth.make_inputs(synth.small_workload(B, [512, 300, 200], k=100, K=160, S_cap=S), seed=5)
+    topk = t["topk_idx"].clone()
+    topk[0, 100:130] = torch.tensor([-5, 512, 513, 10 ** 6, -1] * 6, dtype=torch.int32)
+    topk[1, 100:] = 300 + torch.arange(60, dtype=torch.int32)   # all >= end_pos[1] = 300
+    topk[2, :] = -1       # nothing selected
+    t["topk_idx"] = topk
+    d = _dev(t)
+    x = U.oracle_inputs(t)
+    step = mla.DecodeStep(B, 160)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    step.check_status()
+    got = out.cpu().numpy()
+    assert np.all(got[2] == 0.0)
+    U.assert_attn_close(got[:2], U.oracle_out(x, [0, 1]), "padded rows")
+
+
+def test_nan_poisoned_unselected_rows_do_not_leak():
+    B, S = 2, 700
+    t = synth.make_inputs(synth.small_workload(B, [700, 650], k=200, K=200, S_cap=S), seed=6)
+    x = U.oracle_inputs(t)
+    want = U.oracle_out(x, [0, 1])
+    for b in range(B):
+        keep = torch.zeros(S, dtype=torch.bool)
+        keep[t["topk_idx"][b].long()] = True
+        t["kv_cache"][b][~keep] = float("nan")
+        t["pe_cache"][b][~keep] = float("nan")
+    d = _dev(t)
+    step = mla.DecodeStep(B, 200)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    U.assert_attn_close(out.cpu().numpy(), want, "NaN-poisoned cache")
+
+
+def test_selection_order_does_not_matter():
+    B = 2
+    t = synth.make_inputs(synth.small_workload(B, [900, 900], k=512, K=512, S_cap=900), seed=8)
+    d = _dev(t)
+    step = mla.DecodeStep(B, 512)
+    a = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"]).clone()
+    perm = torch.randperm(512, generator=torch.Generator().manual_seed(1))
+    b = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"][:, perm.cuda()].contiguous(),
+             d["end_pos"])
+    torch.cuda.synchronize()
+    U.assert_attn_close(b.cpu().numpy(), a.cpu().numpy().astype(np.float64), "permuted selection")
+
+
+def test_single_key_and_bad_end_pos_status():
+    B, S = 3, 64
+    t = synth.make_inputs(synth.small_workload(B, [64, 64, 64], k=1, K=1, S_cap=S), seed=9)
+    t["end_pos"] = torch.tensor([64, 0, 65], dtype=torch.int32)   # 0 and > S_cap are invalid
+    d = _dev(t)
+    step = mla.DecodeStep(B, 1)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    st = int(step.status.item())
+    assert st & mla.MLA_DEV_BAD_END_POS
+    got = out.cpu().numpy()
+    assert np.all(got[1] == 0.0) and np.all(got[2] == 0.0)
+    x = U.oracle_inputs(t)
+    tk = int(t["topk_idx"][0, 0])
+    w_uv = x["wkv_b"].reshape(128, 256, 512)[:, 128:, :]
+    want = np.einsum("hdc,c->hd", w_uv, x["kv_cache"][0][tk])
+    U.assert_attn_close(got[0], want, "single key")
+
+
+# ----------------------------------------------------------------- the named workloads, full size
+SAMPLES = {
+    "p1000_b1": [0],
+    "sparse_b32_ctx4096_top2048": [0, 17, 31],
+    "sparse_b64_ctx16384_top2048": [0, 33, 63],
+    "ragged_b128_ctx1024to8192_top2048": None,   # chosen below: shortest, longest, a middle one
+    "dense_b16_ctx16384": [0, 15],
+    "dense_b1_ctx16384": [0],
+}
+
+
+@pytest.mark.parametrize("name", synth.WORKLOADS)
+def test_named_workload_matches_oracle_on_sampled_sequences(name):
+    wl = synth.workload(name)
+    t = synth.make_inputs(wl, seed=0)
+    d = _dev(t)
+    step = mla.DecodeStep(wl.B, wl.row_stride())
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    step.check_status()
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    bs = SAMPLES[name]
+    if bs is None:
+        ep = np.asarray(wl.end_pos)
+        bs = sorted({int(ep.argmin()), int(ep.argmax()), wl.B // 2})
+    x = _oracle_view(t)
+    U.assert_attn_close(got[bs], U.oracle_out(x, bs), name)
