@@ -95,7 +95,7 @@ class ClockSampler:
         self.path = None
         try:
             props = torch.cuda.get_device_properties(device_index)
-            self.bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}"
+            self.bus = f"{props.pci_bus_id:02X}:{props.pci_device_id:02X}."
         except Exception:
             self.bus = None
 
@@ -122,13 +122,13 @@ class ClockSampler:
         try:
             for line in open(self.path):
                 f = [x.strip() for x in line.split(",")]
-                if len(f) < 10:
-                    continue
-                if self.bus and not f[1].upper().endswith(self.bus[-7:]):
-                    continue
-                rows.append(f)
+                if len(f) >= 10:
+                    rows.append(f)
         finally:
             os.unlink(self.path)
+        mine = [r for r in rows if self.bus and self.bus in r[1].upper()]
+        if mine or len({r[0] for r in rows}) > 1:
+            rows = mine
         if not rows:
             return None
 
@@ -222,6 +222,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     st = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
     kt = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    for ev in kt:       # the library re-records these on the launching stream; a first record
+        ev.record()     # through torch marks them recorded for torch's elapsed_time()
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
