@@ -168,6 +168,30 @@ int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla
  * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096). */
 int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, float *out, mla_stream_t stream);
 
+/* mla_sparse_decode_static_ws -- mla_sparse_decode without a caller-supplied
+ * workspace.  The pages have no counterpart to this call; it exists for
+ * callers that cannot allocate device memory (a plugin host that owns every
+ * buffer, a serving loop where an allocator call could stall the device, a
+ * fixed memory plan).  They pass inputs and outputs as for mla_sparse_decode;
+ * the scratch comes from one array of MLA_STATIC_WS_BYTES compiled into the
+ * library's device image (each GPU that loads the library reserves it until
+ * the process exits).  The call allocates nothing.
+ *   - Arguments, layouts and results are those of mla_sparse_decode.
+ *   - Returns MLA_ERR_SIZE when mla_sparse_decode_workspace_size(B, K) is 0
+ *     or exceeds MLA_STATIC_WS_BYTES (e.g. B*128*512*4 bytes of latent output
+ *     alone must fit when wkv_b is given).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero.  Calls whose kernels
+ *     overlap on the GPU (other streams, other host threads) race on it:
+ *     order them on one stream. */
+#define MLA_STATIC_WS_BYTES (32u << 20)
+int mla_sparse_decode_static_ws(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla_bf16 *pe_cache,
+                                int S_cap, const int32_t *topk_idx, int K, const int32_t *end_pos, int B,
+                                float softmax_scale, const mla_bf16 *wkv_b, float *out, int32_t *dev_status,
+                                mla_stream_t stream);
+
 /* Profiling hook for the calling host thread (the library's only mutable
  * state, and it is per thread).  While set:
  *   - every entry point adds the number of kernels it enqueues to

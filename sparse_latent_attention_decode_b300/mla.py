@@ -53,6 +53,7 @@ def _load():
         "mla_out_up": (I, [P, P, I, P, P]),
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_profile_hook": (I, [P, P, P]),
+        "mla_sparse_decode_static_ws": (I, [P, P, P, I, P, I, P, I, F, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -65,7 +66,8 @@ _lib = _load()
 
 EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply",
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
-            "mla_status_string", "mla_profile_hook")
+            "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws")
+STATIC_WS_BYTES = 32 << 20
 
 
 def status_string(code: int) -> str:
@@ -182,6 +184,30 @@ def mla_sparse_decode(q_lat, kv_cache, pe_cache, topk_idx, end_pos, softmax_scal
                                   _ptr(end_pos), B, float(softmax_scale), _ptr(wkv_b), _ptr(out),
                                   _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                   _stream(q_lat.device)), "mla_sparse_decode")
+    return out
+
+
+def mla_sparse_decode_static_ws(q_lat, kv_cache, pe_cache, topk_idx, end_pos, softmax_scale, wkv_b=None, out=None,
+                                dev_status=None) -> torch.Tensor:
+    """mla_sparse_decode for callers that cannot allocate a workspace: the
+    library's own fixed device array (STATIC_WS_BYTES) serves as scratch.
+    Calls that overlap on the GPU share that array and must not race."""
+    B, K = topk_idx.shape
+    S_cap = kv_cache.shape[1]
+    _need(q_lat, "q_lat", torch.bfloat16, (B, N_HEADS, Q_LAT))
+    _need(kv_cache, "kv_cache", torch.bfloat16, (B, S_cap, KV_LORA))
+    _need(pe_cache, "pe_cache", torch.bfloat16, (B, S_cap, D_ROPE))
+    _need(topk_idx, "topk_idx", torch.int32, (B, K))
+    _need(end_pos, "end_pos", torch.int32, (B,))
+    if wkv_b is not None:
+        _need(wkv_b, "wkv_b", torch.bfloat16, (N_HEADS * (D_NOPE + D_V), KV_LORA))
+    width = D_V if wkv_b is not None else KV_LORA
+    if out is None:
+        out = torch.empty(B, N_HEADS, width, dtype=torch.float32, device=q_lat.device)
+    _need(out, "out", torch.float32, (B, N_HEADS, width))
+    _check(_lib.mla_sparse_decode_static_ws(_ptr(q_lat), _ptr(kv_cache), _ptr(pe_cache), S_cap, _ptr(topk_idx), K,
+                                            _ptr(end_pos), B, float(softmax_scale), _ptr(wkv_b), _ptr(out),
+                                            _ptr(dev_status), _stream(q_lat.device)), "mla_sparse_decode_static_ws")
     return out
 
 
