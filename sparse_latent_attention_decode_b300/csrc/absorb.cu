@@ -1,59 +1,146 @@
-// Query of the latent attention: key absorption with the RoPE of q_pe fused in.
+// Query of the latent attention: key absorption on the tensor cores, with the
+// RoPE of q_pe fused in.
 //
 // Source: DeepSeek-V3.2-Exp atlas, "Query content heads" page, excerpt
 // mla-decode (first einsum: q_nope . W_UK per head), and "Rotated query part"
 // page, excerpt apply-rope (pair rotation of q_pe).
+//
+// One CTA per head h computes, in the transposed ("swap-AB") form that puts
+// the 512 latent columns on the 128-row MMA dimension,
+//     q~_h^T [512, B] = W_UK[h]^T [512, 128] . q_nope_h^T [128, B]
+// as four M=128 tiles with N = the batch (up to 128 sequences per pass).
+// W_UK[h] (128 KB) is loaded once by TMA and read MN-major; the batch tile
+// arrives K-major through a 3-D tensor map over q_nope.  Results leave TMEM
+// as bf16 rows of q_lat.
 #include "common.cuh"
+#include "kernels.cuh"
+#include "tc05.cuh"
 
 namespace mla {
+namespace absorb {
 
-constexpr int ABS_BT = 16;  // sequences per CTA
+using namespace tc;
 
-// grid (H, C/128, ceil(B/16)), 128 threads: thread = one latent column c of
-// one head; W_UK[h][d][c] is read once per CTA, coalesced over c.
-__global__ void __launch_bounds__(128) absorb_simt_kernel(
-    const uint16_t *__restrict__ q_nope, const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis,
-    int max_seq_len, const int32_t *__restrict__ end_pos, const uint16_t *__restrict__ wkv_b, int B,
-    uint16_t *__restrict__ q_lat, int32_t *status) {
-    __shared__ float qs[ABS_BT][DN];
-    const int h = blockIdx.x, c = blockIdx.y * 128 + threadIdx.x, b0 = blockIdx.z * ABS_BT;
-    const int nb = min(ABS_BT, B - b0);
-    for (int k = threadIdx.x; k < ABS_BT * DN; k += 128) {
-        const int j = k / DN, d = k % DN;
-        qs[j][d] = j < nb ? bf2f(q_nope[((size_t)(b0 + j) * H + h) * DN + d]) : 0.f;
+constexpr int NMAX = 128;                      // sequences per pass
+constexpr int A_BOX = 128 * 128;               // one [128 d][64 c] box of W_UK, bytes
+constexpr int B_BOX = NMAX * 128;              // one [128 b][64 d] box of q_nope, bytes
+constexpr int SMEM_BYTES = 8 * A_BOX + 2 * B_BOX + 1024;
+constexpr uint64_t TIMEOUT_NS = 2000000000ull;
+
+struct Bars {
+    uint64_t a_full[4], b_full, mma_done;
+    uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(128, 1)
+    absorb_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
+                  const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis, int max_seq_len,
+                  const int32_t *__restrict__ end_pos, int B, uint16_t *__restrict__ q_lat, int32_t *status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ Bars bars;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem, *sB = smem + 8 * A_BOX;
+    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int t = 0; t < 4; ++t) mbar_init(&bars.a_full[t], 1);
+        mbar_init(&bars.b_full, 1);
+        mbar_init(&bars.mma_done, 1);
+        fence_mbar_init();
     }
+    if (warp == 0) {
+        tmem_alloc(&bars.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
-    float acc[ABS_BT];
-#pragma unroll
-    for (int j = 0; j < ABS_BT; ++j) acc[j] = 0.f;
-    const uint16_t *w = wkv_b + (size_t)h * WROWS * C + c;
-    for (int d = 0; d < DN; ++d) {
-        const float wv = bf2f(w[(size_t)d * C]);
-#pragma unroll
-        for (int j = 0; j < ABS_BT; ++j) acc[j] = fmaf(qs[j][d], wv, acc[j]);
-    }
-    for (int j = 0; j < nb; ++j) q_lat[((size_t)(b0 + j) * H + h) * QL + c] = f2bf(acc[j]);
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
+    bool ok = true;
 
-    // fused RoPE prologue: the c-chunk-0 CTA of each head rotates q_pe
-    if (blockIdx.y == 0 && threadIdx.x < NPAIR) {
-        const int i = threadIdx.x;
-        for (int j = 0; j < nb; ++j) {
-            const int b = b0 + j;
-            const int pos = end_pos[b] - 1;
-            uint32_t packed = 0;
-            if (pos >= 0 && pos < max_seq_len) {
-                const uint32_t wv = reinterpret_cast<const uint32_t *>(q_pe + ((size_t)b * H + h) * DR)[i];
-                const float x0 = bflo(wv), x1 = bfhi(wv);
-                const float2 cs = cis[(size_t)pos * NPAIR + i];
-                packed = uint32_t(f2bf(x0 * cs.x - x1 * cs.y)) | (uint32_t(f2bf(x0 * cs.y + x1 * cs.x)) << 16);
-            } else if (i == 0 && h == 0) {
-                report(status, MLA_DEV_BAD_POSITION);
-            }
-            reinterpret_cast<uint32_t *>(q_lat + ((size_t)b * H + h) * QL + C)[i] = packed;
+    if (tid == 0) {
+        // W_UK[h] = rows h*256 .. h*256+127 of wkv_b; tile t = latent columns 128t .. 128t+127
+        for (int t = 0; t < 4; ++t) {
+            mbar_expect_tx(&bars.a_full[t], 2 * A_BOX);
+            tma_load_2d(smem_u32(sA + (2 * t) * A_BOX), &wmap, 128 * t, h * WROWS, &bars.a_full[t]);
+            tma_load_2d(smem_u32(sA + (2 * t + 1) * A_BOX), &wmap, 128 * t + 64, h * WROWS, &bars.a_full[t]);
         }
+    }
+
+    const int npass = (B + NMAX - 1) / NMAX;
+    for (int pass = 0; pass < npass && ok; ++pass) {
+        const int n0 = pass * NMAX;
+        const int nb = min(NMAX, B - n0);
+        const int N = (nb + 15) & ~15;
+        if (tid == 0) {
+            mbar_expect_tx(&bars.b_full, 2 * B_BOX);
+            tma_load_3d(smem_u32(sB), &qmap, 0, h, n0, &bars.b_full);
+            tma_load_3d(smem_u32(sB + B_BOX), &qmap, 64, h, n0, &bars.b_full);
+            bool good = wait_until(&bars.b_full, pass & 1, deadline);
+            const uint32_t idesc = idesc_bf16(128, N, true, false);
+            for (int t = 0; t < 4 && good; ++t) {
+                if (pass == 0) good = wait_until(&bars.a_full[t], 0, deadline);
+                if (!good) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = smem_desc(smem_u32(sA + (2 * t) * A_BOX) + kk * 2048, A_BOX, 1024, 2);
+                    const uint64_t bd = smem_desc(smem_u32(sB + (kk >> 2) * B_BOX) + (kk & 3) * 32, 16, 1024, 2);
+                    mma_ss(tmem + t * NMAX, ad, bd, idesc, kk > 0);
+                }
+            }
+            if (good) mma_commit(&bars.mma_done);
+            else report(status, MLA_DEV_TIMEOUT);
+        }
+        ok = __syncthreads_and(wait_until(&bars.mma_done, pass & 1, deadline));
+        if (!ok) break;
+        tc_fence_after();
+        // epilogue: lane = latent column within the tile, column = sequence
+        const uint32_t trow = tmem + (uint32_t(32 * warp) << 16);
+        for (int t = 0; t < 4; ++t) {
+            for (int j0 = 0; j0 < N; j0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(trow + t * NMAX + j0, v);
+                tmem_ld_wait();
+                const int c = 128 * t + 32 * warp + lane;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int b = n0 + j0 + i;
+                    if (b < B) q_lat[((size_t)b * H + h) * QL + c] = f2bf(__uint_as_float(v[i]));
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();   // TMEM and the batch tile are reused by the next pass
+    }
+    if (!ok && tid == 0) report(status, MLA_DEV_TIMEOUT);
+
+    // fused RoPE of q_pe: thread = (pair, sequence)
+    for (int k = tid; k < B * NPAIR; k += 128) {
+        const int b = k / NPAIR, i = k % NPAIR;
+        const int pos = end_pos[b] - 1;
+        uint32_t packed = 0;
+        if (pos >= 0 && pos < max_seq_len) {
+            const uint32_t w = reinterpret_cast<const uint32_t *>(q_pe + ((size_t)b * H + h) * DR)[i];
+            const float x0 = bflo(w), x1 = bfhi(w);
+            const float2 cs = cis[(size_t)pos * NPAIR + i];
+            packed = uint32_t(f2bf(x0 * cs.x - x1 * cs.y)) | (uint32_t(f2bf(x0 * cs.y + x1 * cs.x)) << 16);
+        } else if (i == 0 && h == 0) {
+            report(status, MLA_DEV_BAD_POSITION);
+        }
+        reinterpret_cast<uint32_t *>(q_lat + ((size_t)b * H + h) * QL + C)[i] = packed;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
     }
 }
 
+}  // namespace absorb
 }  // namespace mla
 
 using namespace mla;
@@ -65,9 +152,31 @@ extern "C" int mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const 
     if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(cis) || !aligned16(wkv_b) || !aligned16(q_lat))
         return MLA_ERR_ALIGN;
     if (B < 1 || B > 4096 || max_seq_len < 1) return MLA_ERR_SIZE;
-    dim3 grid(H, C / 128, (B + ABS_BT - 1) / ABS_BT);
-    absorb_simt_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(q_nope, q_pe, reinterpret_cast<const float2 *>(cis),
-                                                              max_seq_len, end_pos, wkv_b, B, q_lat, dev_status);
+    CUtensorMap wmap, qmap;
+    {
+        const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
+        const uint64_t strides[1] = {(uint64_t)C * 2};
+        const uint32_t box[2] = {64, 128};
+        if (!make_tmap_bf16(&wmap, wkv_b, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[3] = {(uint64_t)DN, (uint64_t)H, (uint64_t)B};
+        const uint64_t strides[2] = {(uint64_t)DN * 2, (uint64_t)H * DN * 2};
+        const uint32_t box[3] = {64, 1, absorb::NMAX};
+        if (!make_tmap_bf16(&qmap, q_nope, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        if (cudaFuncSetAttribute(absorb::absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 absorb::SMEM_BYTES) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    absorb::absorb_kernel<<<H, 128, absorb::SMEM_BYTES, s>>>(wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis),
+                                                            max_seq_len, end_pos, B, q_lat, dev_status);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

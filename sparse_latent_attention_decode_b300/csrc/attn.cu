@@ -1,5 +1,5 @@
 // Sparse latent attention on the 5th-generation tensor cores (tcgen05 + TMEM),
-// fed by TMA row gathers.
+// fed by 16-byte cp.async row gathers.
 //
 // Source: DeepSeek-V3.2-Exp atlas, "Attention weights" page, excerpt
 // mla-decode: scores = (q~ . kv + q_pe . pe) * scale over the cached rows,
@@ -35,19 +35,33 @@ namespace attn {
 using namespace tc;
 
 constexpr int NK = 64;                       // keys per block
-constexpr int NS = 4;                        // gather pipeline stages
+constexpr int NS = 5;                        // gather pipeline stages
 constexpr int STAGE_KV = 4 * NK * 128;       // 4 atom columns of 64 latent x 64 keys (128B swizzle)
 constexpr int STAGE_PE = NK * 64;            // 32 rotary columns x 64 keys (64B swizzle)
 constexpr int STAGE = STAGE_KV + STAGE_PE;   // 36864
 constexpr int RECV = H * NK * 2;             // fp16 partial scores of the peer, 128 x 64
 constexpr int SMEM_BYTES = NS * STAGE + 2 * RECV + 1024;
 constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 400, P_COL = 464, TMEM_COLS = 512;
-constexpr int THREADS = 192;                 // warp 0 gather, warp 1 MMA, warps 2..5 softmax
+// warps 0..7 gather (cp.async), 8..11 softmax, 12 MMA, 13..15 idle: four
+// warpgroups, so that registers can move from the gather warps to the softmax
+constexpr int THREADS = 512;
+constexpr int GATHER_THREADS = 256;
+constexpr int CHUNKS = NK * 36;              // 16-byte chunks per stage: 32 latent + 4 rotary per key
+constexpr int CHUNKS_PER_THREAD = CHUNKS / GATHER_THREADS;   // 9
+constexpr int MMA_WARP = 12;
+// A gather thread publishes block j once it has issued block j+LAG and the
+// copies of block j have landed.  The MMA issues QK two blocks ahead of PV, so
+// block j+2 must be published without waiting for a stage that PV(j) frees:
+// (j + 2 + LAG) - NS < j, i.e. LAG <= NS - 3.
+constexpr int LAG = 2;
+static_assert(LAG <= NS - 3, "gather publication lag would deadlock against the QK lookahead");
 constexpr float RESCALE_T = 8.f;             // lazy-max threshold (log2 units)
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
 struct Params {
     const uint16_t *q_lat;
+    const uint16_t *kv;
+    const uint16_t *pe;
     const int32_t *topk;
     const int32_t *end_pos;
     int S_cap, K, B;
@@ -76,8 +90,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity
     return __all_sync(0xffffffffu, wait_until_cluster(bar, parity, deadline));
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap pemap, Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_kernel(Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -96,7 +109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (!seq_ok && tid == 0 && r == 0 && split == 0) report(p.status, MLA_DEV_BAD_END_POS);
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(&bars.full[s], 1), mbar_init(&bars.empty[s], 1);
+        for (int s = 0; s < NS; ++s) mbar_init(&bars.full[s], GATHER_THREADS), mbar_init(&bars.empty[s], 1);
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.s_free, 128);
         mbar_init(&bars.p_full, 128);
@@ -105,7 +118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int k = 0; k < 2; ++k) mbar_init(&bars.recv_full[k], 128), mbar_init(&bars.send_credit[k], 128);
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == MMA_WARP) {
         tmem_alloc(&bars.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
@@ -115,49 +128,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t tmem = bars.tmem_base;
     const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ gather producer
-        const int row_base = b * p.S_cap;
-        const int oob = p.B * p.S_cap;   // first row past the tensor: the TMA fills zeros
+    if (warp < 8) {
+        // ------------------------------------------------------------ gather producers
+        // 256 threads copy a stage's 2304 16-byte chunks with cp.async, 9 each.
+        // Chunk e = tid + 256 q belongs to key e / 36; chunks 0..31 of a key are
+        // its latent half (4 atom columns x 8, 128-byte swizzle), 32..35 its
+        // rotary half (64-byte swizzle).  Invalid keys are zero-filled.
+        regs_dec<96>();
+        uint32_t dst_off[CHUNKS_PER_THREAD];
+        int src_off[CHUNKS_PER_THREAD], key[CHUNKS_PER_THREAD];
+        bool is_pe[CHUNKS_PER_THREAD];
+#pragma unroll
+        for (int q = 0; q < CHUNKS_PER_THREAD; ++q) {
+            const int ch = tid + GATHER_THREADS * q;
+            key[q] = ch / 36;
+            const int c = ch % 36;
+            is_pe[q] = c >= 32;
+            if (c < 32) {
+                const int a = c >> 3, cc = c & 7;
+                dst_off[q] = a * (NK * 128) + sw128(key[q], cc);
+                src_off[q] = 256 * r + 64 * a + 8 * cc;
+            } else {
+                const int cc = c - 32;
+                dst_off[q] = STAGE_KV + sw64(key[q], cc);
+                src_off[q] = 32 * r + 8 * cc;
+            }
+        }
+        const uint16_t *kvb = p.kv + (size_t)b * p.S_cap * C;
+        const uint16_t *peb = p.pe + (size_t)b * p.S_cap * DR;
         const int32_t *sel = p.topk + (size_t)b * p.K;
+        int cur[CHUNKS_PER_THREAD], nxt[CHUNKS_PER_THREAD];
+        auto load_idx = [&](int j, int(&dst)[CHUNKS_PER_THREAD]) {
+#pragma unroll
+            for (int q = 0; q < CHUNKS_PER_THREAD; ++q) {
+                const int slot = t0 + j * NK + key[q];
+                const int id = slot < t1 ? sel[slot] : -1;
+                dst[q] = (id >= 0 && id < e) ? id : -1;
+            }
+        };
+        if (nblk > 0) load_idx(0, nxt);
         int j = 0;
         for (; j < nblk; ++j) {
+#pragma unroll
+            for (int q = 0; q < CHUNKS_PER_THREAD; ++q) cur[q] = nxt[q];
+            if (j + 1 < nblk) load_idx(j + 1, nxt);   // prefetch: used next iteration
             const int s = j % NS;
             if (j >= NS && !warp_wait(&bars.empty[s], ((j / NS) - 1) & 1, deadline)) {
                 fail(p);
                 break;
             }
-            const int slot = t0 + j * NK + 2 * lane;
-            const int i0 = slot < t1 ? sel[slot] : -1;
-            const int i1 = slot + 1 < t1 ? sel[slot + 1] : -1;
-            const int ra = (i0 >= 0 && i0 < e) ? row_base + i0 : oob;
-            const int rb = (i1 >= 0 && i1 < e) ? row_base + i1 : oob;
-            // quad g holds keys 4g..4g+3 = (ra, rb) of lanes 2g and 2g+1
-            const int g = lane & 15;
-            const int q0 = __shfl_sync(0xffffffffu, ra, 2 * g), q1 = __shfl_sync(0xffffffffu, rb, 2 * g);
-            const int q2 = __shfl_sync(0xffffffffu, ra, 2 * g + 1), q3 = __shfl_sync(0xffffffffu, rb, 2 * g + 1);
-            if (lane == 0) mbar_expect_tx(&bars.full[s], STAGE);
-            __syncwarp();
-            if (lane < 16) {
-                const uint32_t dst = smem_u32(stages + s * STAGE);
+            const uint32_t base = smem_u32(stages + s * STAGE);
 #pragma unroll
-                for (int a = 0; a < 4; ++a)
-                    tma_gather4(dst + a * (NK * 128) + g * 512, &kvmap, 256 * r + 64 * a, q0, q1, q2, q3,
-                                &bars.full[s]);
-                tma_gather4(dst + STAGE_KV + g * 256, &pemap, 32 * r, q0, q1, q2, q3, &bars.full[s]);
+            for (int q = 0; q < CHUNKS_PER_THREAD; ++q) {
+                const int row = cur[q] < 0 ? 0 : cur[q];
+                const uint16_t *src = is_pe[q] ? peb + (size_t)row * DR + src_off[q] : kvb + (size_t)row * C + src_off[q];
+                cp_async16(base + dst_off[q], src, cur[q] < 0 ? 0u : 16u);
             }
-            __syncwarp();
+            cp_async_commit();
+            if (j >= LAG) {   // the copies of block j-LAG have landed: publish them
+                cp_async_wait<LAG>();
+                fence_proxy_async_smem();
+                mbar_arrive(&bars.full[(j - LAG) % NS]);
+            }
         }
-        // no copy may still be landing in shared memory when the CTA exits
-        if (lane == 0)
-            for (int jj = max(0, j - NS); jj < j; ++jj)
-                if (!wait_until(&bars.full[jj % NS], (jj / NS) & 1, deadline)) {
-                    fail(p);
-                    break;
-                }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && nblk > 0) {
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (int jj = max(0, j - LAG); jj < j; ++jj) mbar_arrive(&bars.full[jj % NS]);
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ MMA issuer (warp 12, one thread)
+        regs_dec<64>();
+        if (warp == MMA_WARP && lane == 0 && nblk > 0) {
             bool ok = wait_until(&bars.q_ready, 0, deadline);
             tc_fence_after();
             constexpr uint32_t idesc_qk = idesc_bf16(128, NK, false, false);
@@ -192,15 +232,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 mma_commit(&bars.empty[s]);
                 return true;
             };
+            // QK runs two blocks ahead of PV: the softmax of block j overlaps QK(j+1)
             ok = ok && issue_qk(0);
+            if (nblk > 1) ok = ok && issue_qk(1);
             for (int j = 0; ok && j < nblk; ++j) {
-                if (j + 1 < nblk) ok = issue_qk(j + 1);
+                if (j + 2 < nblk) ok = issue_qk(j + 2);
                 ok = ok && issue_pv(j);
             }
             if (!ok) fail(p);
         }
     } else {
         // ------------------------------------------------------------ softmax warps (one thread per head)
+        regs_inc<232>();
         const int quad = warp & 3;
         const int h = 32 * quad + lane;
         const uint32_t trow = tmem + (uint32_t(32 * quad) << 16);
@@ -227,117 +270,130 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t recv_local = smem_u32(recv);
         const uint32_t recv_peer = map_peer(recv_local, peer);
         const int32_t *sel = p.topk + (size_t)b * p.K;
-        for (int j = 0; j < nblk && ok; ++j) {
-            // validity of the block's 64 keys (key k: bit k)
-            const int slot = t0 + j * NK + 2 * lane;
-            const int i0 = slot < t1 ? sel[slot] : -1;
-            const int i1 = slot + 1 < t1 ? sel[slot + 1] : -1;
-            const uint32_t ve = __ballot_sync(0xffffffffu, i0 >= 0 && i0 < e);
-            const uint32_t vo = __ballot_sync(0xffffffffu, i1 >= 0 && i1 < e);
+        // Iteration j loads block j's partial scores and sends them to the peer,
+        // then finishes block j-1, whose peer half arrived during the previous
+        // iteration: the exchange latency hides behind a block of work.
+        float xp[NK];
+        uint32_t vpe = 0, vpo = 0;
+        for (int j = 0; j <= nblk && ok; ++j) {
+            float xc[NK];
+            uint32_t vce = 0, vco = 0;
+            if (j < nblk) {
+                // validity of the block's 64 keys (key k: bit k/2 of vce for even k, of vco for odd k)
+                const int slot = t0 + j * NK + 2 * lane;
+                const int i0 = slot < t1 ? sel[slot] : -1;
+                const int i1 = slot + 1 < t1 ? sel[slot + 1] : -1;
+                vce = __ballot_sync(0xffffffffu, i0 >= 0 && i0 < e);
+                vco = __ballot_sync(0xffffffffu, i1 >= 0 && i1 < e);
 
-            if (!warp_wait(&bars.s_full, j & 1, deadline)) { ok = false; break; }
-            tc_fence_after();
-            float x[NK];
-            {
-                uint32_t v[16];
+                if (!warp_wait(&bars.s_full, j & 1, deadline)) { ok = false; break; }
+                tc_fence_after();
+                {
+                    uint32_t v[16];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld16(trow + S_COL + 16 * c, v);
-                    tmem_ld_wait();
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld16(trow + S_COL + 16 * c, v);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) x[16 * c + i] = __uint_as_float(v[i]) * p.scale_log2;
+                        for (int i = 0; i < 16; ++i) xc[16 * c + i] = __uint_as_float(v[i]) * p.scale_log2;
+                    }
                 }
-            }
-            tc_fence_before();
-            mbar_arrive(&bars.s_free);
+                tc_fence_before();
+                mbar_arrive(&bars.s_free);
 
-            // send my partial scores (fp16) into the peer's receive buffer j&1
-            const int kb = j & 1;
-            if (j >= 2 && !warp_wait_cluster(&bars.send_credit[kb], ((j >> 1) - 1) & 1, deadline)) {
-                ok = false;
-                break;
-            }
-            {
+                // send my partial scores (fp16) into the peer's receive buffer j&1
+                const int kb = j & 1;
+                if (j >= 2 && !warp_wait_cluster(&bars.send_credit[kb], ((j >> 1) - 1) & 1, deadline)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t dst = recv_peer + kb * RECV + h * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    st_cluster_v4(dst + ((c ^ (h & 7)) << 4), pack_f16_sat(x[8 * c], x[8 * c + 1]),
-                                  pack_f16_sat(x[8 * c + 2], x[8 * c + 3]), pack_f16_sat(x[8 * c + 4], x[8 * c + 5]),
-                                  pack_f16_sat(x[8 * c + 6], x[8 * c + 7]));
+                    st_cluster_v4(dst + ((c ^ (h & 7)) << 4), pack_f16_sat(xc[8 * c], xc[8 * c + 1]),
+                                  pack_f16_sat(xc[8 * c + 2], xc[8 * c + 3]), pack_f16_sat(xc[8 * c + 4], xc[8 * c + 5]),
+                                  pack_f16_sat(xc[8 * c + 6], xc[8 * c + 7]));
                 mbar_arrive_cluster(&bars.recv_full[kb], peer);
             }
-            if (!warp_wait_cluster(&bars.recv_full[kb], (j >> 1) & 1, deadline)) { ok = false; break; }
-            {
-                const uint32_t src = recv_local + kb * RECV + h * 128;
+            if (j >= 1) {
+                const int jp = j - 1, kp = jp & 1;
+                if (!warp_wait_cluster(&bars.recv_full[kp], (jp >> 1) & 1, deadline)) { ok = false; break; }
+                {
+                    const uint32_t src = recv_local + kp * RECV + h * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t a0, a1, a2, a3;
-                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                                 : "r"(src + ((c ^ (h & 7)) << 4)));
-                    const float2 f0 = unpack_f16(a0), f1 = unpack_f16(a1), f2 = unpack_f16(a2), f3 = unpack_f16(a3);
-                    x[8 * c] += f0.x, x[8 * c + 1] += f0.y, x[8 * c + 2] += f1.x, x[8 * c + 3] += f1.y;
-                    x[8 * c + 4] += f2.x, x[8 * c + 5] += f2.y, x[8 * c + 6] += f3.x, x[8 * c + 7] += f3.y;
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t a0, a1, a2, a3;
+                        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                                     : "r"(src + ((c ^ (h & 7)) << 4)));
+                        const float2 f0 = unpack_f16(a0), f1 = unpack_f16(a1), f2 = unpack_f16(a2), f3 = unpack_f16(a3);
+                        xp[8 * c] += f0.x, xp[8 * c + 1] += f0.y, xp[8 * c + 2] += f1.x, xp[8 * c + 3] += f1.y;
+                        xp[8 * c + 4] += f2.x, xp[8 * c + 5] += f2.y, xp[8 * c + 6] += f3.x, xp[8 * c + 7] += f3.y;
+                    }
+                    mbar_arrive_cluster(&bars.send_credit[kp], peer);   // the peer may refill this buffer
                 }
-                mbar_arrive_cluster(&bars.send_credit[kb], peer);   // the peer may refill this buffer
-            }
 
-            // online softmax over the block (lazy maximum)
-            float bm = -INFINITY;
+                // online softmax over block jp (lazy maximum)
+                float bm = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < NK; ++i) {
-                const bool valid = ((i & 1) ? (vo >> (i >> 1)) : (ve >> (i >> 1))) & 1u;
-                x[i] = valid ? x[i] : -INFINITY;
-                bm = fmaxf(bm, x[i]);
-            }
-            float f = 1.f;
-            if (bm > m + RESCALE_T) {
-                f = ex2(m - bm);   // m = -inf -> 0
-                m = bm;
-            }
-            uint32_t pk[NK / 2];
-            float sum = 0.f;
+                for (int i = 0; i < NK; ++i) {
+                    const bool valid = ((i & 1) ? (vpo >> (i >> 1)) : (vpe >> (i >> 1))) & 1u;
+                    xp[i] = valid ? xp[i] : -INFINITY;
+                    bm = fmaxf(bm, xp[i]);
+                }
+                float f = 1.f;
+                if (bm > m + RESCALE_T) {
+                    f = ex2(m - bm);   // m = -inf -> 0
+                    m = bm;
+                }
+                uint32_t pk[NK / 2];
+                float sum = 0.f;
 #pragma unroll
-            for (int i = 0; i < NK; i += 2) {
-                const float p0 = ex2(x[i] - m), p1 = ex2(x[i + 1] - m);   // -inf -> 0
-                sum += p0 + p1;
-                pk[i / 2] = pack_bf16(p0, p1);
-            }
-            if (m == -INFINITY) {   // nothing valid so far: P must be zero, not NaN
-                sum = 0.f;
+                for (int i = 0; i < NK; i += 2) {
+                    const float p0 = ex2(xp[i] - m), p1 = ex2(xp[i + 1] - m);   // -inf -> 0
+                    sum += p0 + p1;
+                    pk[i / 2] = pack_bf16(p0, p1);
+                }
+                if (m == -INFINITY) {   // nothing valid so far: P must be zero, not NaN
+                    sum = 0.f;
 #pragma unroll
-                for (int i = 0; i < NK / 2; ++i) pk[i] = 0u;
-            }
-            l = l * f + sum;
+                    for (int i = 0; i < NK / 2; ++i) pk[i] = 0u;
+                }
+                l = l * f + sum;
 
-            // P and O are in use by PV(j-1) until it completes
-            if (j > 0) {
-                if (!warp_wait(&bars.pv_done, (j - 1) & 1, deadline)) { ok = false; break; }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, f != 1.f)) {
+                // P and O are in use by PV(jp-1) until it completes
+                if (jp > 0) {
+                    if (!warp_wait(&bars.pv_done, (jp - 1) & 1, deadline)) { ok = false; break; }
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 256; c0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(trow + O_COL + c0, v);
-                        tmem_ld_wait();
+                        for (int c0 = 0; c0 < 256; c0 += 16) {
+                            uint32_t v[16];
+                            tmem_ld16(trow + O_COL + c0, v);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                        tmem_st16(trow + O_COL + c0, v);
+                            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                            tmem_st16(trow + O_COL + c0, v);
+                        }
                     }
                 }
-            }
-            {
-                uint32_t v[16];
+                {
+                    uint32_t v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = pk[i];
-                tmem_st16(trow + P_COL, v);
+                    for (int i = 0; i < 16; ++i) v[i] = pk[i];
+                    tmem_st16(trow + P_COL, v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = pk[16 + i];
-                tmem_st16(trow + P_COL + 16, v);
+                    for (int i = 0; i < 16; ++i) v[i] = pk[16 + i];
+                    tmem_st16(trow + P_COL + 16, v);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars.p_full);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bars.p_full);
+#pragma unroll
+            for (int i = 0; i < NK; ++i) xp[i] = xc[i];
+            vpe = vce;
+            vpo = vco;
         }
         if (ok && nblk > 0) {
             if (!warp_wait(&bars.pv_done, (nblk - 1) & 1, deadline)) ok = false;
@@ -374,7 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -436,21 +492,10 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
                 cudaStream_t s, int *launches) {
     int n_split = 1, split_len = K;
     attn_workspace(B, K, &n_split, &split_len);
-    CUtensorMap kvmap, pemap;
-    {
-        const uint64_t dims[2] = {(uint64_t)C, (uint64_t)B * S_cap};
-        const uint64_t strides[1] = {(uint64_t)C * 2};
-        const uint32_t box[2] = {64, 1};
-        if (!make_tmap_bf16(&kvmap, kv, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
-    }
-    {
-        const uint64_t dims[2] = {(uint64_t)DR, (uint64_t)B * S_cap};
-        const uint64_t strides[1] = {(uint64_t)DR * 2};
-        const uint32_t box[2] = {32, 1};
-        if (!make_tmap_bf16(&pemap, pe, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B)) return MLA_ERR_CUDA;
-    }
     attn::Params p{};
     p.q_lat = q_lat;
+    p.kv = kv;
+    p.pe = pe;
     p.topk = topk;
     p.end_pos = end_pos;
     p.S_cap = S_cap;
@@ -479,7 +524,7 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
     const ProfileHook &hook = profile_hook();
     const bool timed = hook.start && hook.stop;
     if (timed && cudaEventRecord(hook.start, s) != cudaSuccess) return MLA_ERR_CUDA;
-    attn::attn_kernel<<<2 * B * n_split, attn::THREADS, attn::SMEM_BYTES, s>>>(kvmap, pemap, p);
+    attn::attn_kernel<<<2 * B * n_split, attn::THREADS, attn::SMEM_BYTES, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     if (timed && cudaEventRecord(hook.stop, s) != cudaSuccess) return MLA_ERR_CUDA;
     int n = 1;

@@ -52,7 +52,7 @@ extern "C" int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache
                          ws + L.attn, dev_status, s, &launches);
     count_launches(launches);
     if (rc != MLA_OK) return rc;
-    if (wkv_b) return launch_out_up(o_lat, wkv_b, B, out, s);
+    if (wkv_b) return launch_out_up(o_lat, wkv_b, B, out, dev_status, s);
     return MLA_OK;
 }
 

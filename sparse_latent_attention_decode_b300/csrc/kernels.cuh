@@ -7,7 +7,7 @@
 
 namespace mla {
 
-int launch_out_up(const float *o_lat, const uint16_t *wkv_b, int B, float *out, cudaStream_t s);
+int launch_out_up(const float *o_lat, const uint16_t *wkv_b, int B, float *out, int32_t *status, cudaStream_t s);
 
 // Sparse attention (tensor-core kernel + split combine).  Writes the
 // normalised latent output o [B][128][512] fp32 to o_out.  ws must hold

@@ -1,52 +1,144 @@
-// Value up-projection: out[b,h,d] = sum_c o[b,h,c] * W_UV[h][d][c].
+// Value up-projection on the tensor cores: out[b,h,d] = sum_c o[b,h,c] * W_UV[h][d][c].
 //
 // Source: DeepSeek-V3.2-Exp atlas, "Attention weights" page, excerpt
 // mla-decode (last einsum, wkv_b[:, -v_head_dim:]).
+//
+// One CTA per head h computes out_h^T [128 d, B] = W_UV[h] [128, 512] . o_h^T
+// [512, B] ("swap-AB": the head's 128 output features fill the MMA rows, the
+// batch is N).  W_UV[h] (128 KB) is loaded once by TMA (K-major); the latent
+// outputs o (fp32) are rounded to bf16 while they are written into the
+// 128-byte-swizzled operand tile, 64 sequences per pass.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tc05.cuh"
 
 namespace mla {
+namespace outup {
 
-constexpr int UP_BT = 8;   // sequences per CTA
-constexpr int UP_CK = 64;  // latent columns per smem tile
+using namespace tc;
 
-// grid (H, ceil(B/8)), 128 threads: thread = one output feature d of one head.
-// o is rounded to bf16 before the product (the operands are bf16; fp32 sums).
-__global__ void __launch_bounds__(128) out_up_simt_kernel(const float *__restrict__ o_lat,
-                                                          const uint16_t *__restrict__ wkv_b, int B,
-                                                          float *__restrict__ out) {
-    __shared__ uint32_t ws[DV][UP_CK / 2 + 1];
-    __shared__ float os[UP_BT][UP_CK];
-    const int h = blockIdx.x, b0 = blockIdx.y * UP_BT, d = threadIdx.x;
-    const int nb = min(UP_BT, B - b0);
-    float acc[UP_BT];
-#pragma unroll
-    for (int j = 0; j < UP_BT; ++j) acc[j] = 0.f;
-    const uint32_t *w_uv = reinterpret_cast<const uint32_t *>(wkv_b + ((size_t)h * WROWS + DN) * C);
-    for (int c0 = 0; c0 < C; c0 += UP_CK) {
-        for (int u = threadIdx.x; u < DV * UP_CK / 2; u += 128) {
-            const int r = u / (UP_CK / 2), w = u % (UP_CK / 2);
-            ws[r][w] = w_uv[(size_t)r * (C / 2) + c0 / 2 + w];
-        }
-        for (int u = threadIdx.x; u < UP_BT * UP_CK; u += 128) {
-            const int j = u / UP_CK, c = u % UP_CK;
-            os[j][c] = j < nb ? bf2f(f2bf(o_lat[((size_t)(b0 + j) * H + h) * C + c0 + c])) : 0.f;
-        }
-        __syncthreads();
-        for (int w = 0; w < UP_CK / 2; ++w) {
-            const uint32_t kw = ws[d][w];
-            const float lo = bflo(kw), hi = bfhi(kw);
-#pragma unroll
-            for (int j = 0; j < UP_BT; ++j) acc[j] = fmaf(os[j][2 * w + 1], hi, fmaf(os[j][2 * w], lo, acc[j]));
-        }
-        __syncthreads();
+constexpr int NMAX = 64;                       // sequences per pass
+constexpr int A_BOX = 128 * 128;               // [128 d][64 c] box of W_UV, bytes
+constexpr int B_ATOM = NMAX * 128;             // [64 b][64 c] atom column of the o tile, bytes
+constexpr int SMEM_BYTES = 8 * A_BOX + 8 * B_ATOM + 1024;
+constexpr uint64_t TIMEOUT_NS = 2000000000ull;
+
+struct Bars {
+    uint64_t a_full, mma_done;
+    uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                        const float *__restrict__ o_lat, int B,
+                                                        float *__restrict__ out, int32_t *status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ Bars bars;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem, *sB = smem + 8 * A_BOX;
+    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        mbar_init(&bars.a_full, 1);
+        mbar_init(&bars.mma_done, 1);
+        fence_mbar_init();
     }
-    for (int j = 0; j < nb; ++j) out[((size_t)(b0 + j) * H + h) * DV + d] = acc[j];
+    if (warp == 0) {
+        tmem_alloc(&bars.tmem_base, NMAX);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
+
+    if (tid == 0) {   // W_UV[h] = rows h*256+128 .. h*256+255 of wkv_b, 8 boxes of 64 latent columns
+        mbar_expect_tx(&bars.a_full, 8 * A_BOX);
+        for (int a = 0; a < 8; ++a)
+            tma_load_2d(smem_u32(sA + a * A_BOX), &wmap, 64 * a, h * WROWS + DN, &bars.a_full);
+    }
+
+    bool ok = true;
+    const int npass = (B + NMAX - 1) / NMAX;
+    for (int pass = 0; pass < npass && ok; ++pass) {
+        const int n0 = pass * NMAX;
+        const int nb = min(NMAX, B - n0);
+        const int N = (nb + 15) & ~15;
+        // o rows of this pass -> bf16 operand tile: 16-byte chunk (row, c/8), 64 chunks per row
+        for (int u = tid; u < N * 64; u += 128) {
+            const int row = u >> 6, ch = u & 63;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row < nb) {
+                const float4 *src = reinterpret_cast<const float4 *>(o_lat + ((size_t)(n0 + row) * H + h) * C + ch * 8);
+                const float4 x0 = src[0], x1 = src[1];
+                w = make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
+                               pack_bf16(x1.z, x1.w));
+            }
+            *reinterpret_cast<uint4 *>(sB + (ch >> 3) * B_ATOM + sw128(row, ch & 7)) = w;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            bool good = pass > 0 || wait_until(&bars.a_full, 0, deadline);
+            if (good) {
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16(128, N, false, false);
+#pragma unroll 4
+                for (int kk = 0; kk < 32; ++kk) {
+                    const uint64_t ad = smem_desc(smem_u32(sA + (kk >> 2) * A_BOX) + (kk & 3) * 32, 16, 1024, 2);
+                    const uint64_t bd = smem_desc(smem_u32(sB + (kk >> 2) * B_ATOM) + (kk & 3) * 32, 16, 1024, 2);
+                    mma_ss(tmem, ad, bd, idesc, kk > 0);
+                }
+                mma_commit(&bars.mma_done);
+            } else {
+                report(status, MLA_DEV_TIMEOUT);
+            }
+        }
+        ok = __syncthreads_and(wait_until(&bars.mma_done, pass & 1, deadline));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t trow = tmem + (uint32_t(32 * warp) << 16);
+        const int d = 32 * warp + lane;
+        for (int j0 = 0; j0 < N; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(trow + j0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int b = n0 + j0 + i;
+                if (b < B) out[((size_t)b * H + h) * DV + d] = __uint_as_float(v[i]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();   // TMEM and the operand tile are reused by the next pass
+    }
+    if (!ok && tid == 0) report(status, MLA_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, NMAX);
+    }
 }
 
-int launch_out_up(const float *o_lat, const uint16_t *wkv_b, int B, float *out, cudaStream_t s) {
-    dim3 grid(H, (B + UP_BT - 1) / UP_BT);
-    out_up_simt_kernel<<<grid, 128, 0, s>>>(o_lat, wkv_b, B, out);
+}  // namespace outup
+
+int launch_out_up(const float *o_lat, const uint16_t *wkv_b, int B, float *out, int32_t *status, cudaStream_t s) {
+    CUtensorMap wmap;
+    const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
+    const uint64_t strides[1] = {(uint64_t)C * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!make_tmap_bf16(&wmap, wkv_b, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        if (cudaFuncSetAttribute(outup::out_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 outup::SMEM_BYTES) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    outup::out_up_kernel<<<H, 128, outup::SMEM_BYTES, s>>>(wmap, o_lat, B, out, status);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -59,5 +151,5 @@ extern "C" int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, floa
     if (!o_lat || !wkv_b || !out) return MLA_ERR_NULL;
     if (!aligned16(o_lat) || !aligned16(wkv_b) || !aligned16(out)) return MLA_ERR_ALIGN;
     if (B < 1 || B > 4096) return MLA_ERR_SIZE;
-    return launch_out_up(o_lat, wkv_b, B, out, (cudaStream_t)stream);
+    return launch_out_up(o_lat, wkv_b, B, out, nullptr, (cudaStream_t)stream);
 }

@@ -191,6 +191,11 @@ __device__ __forceinline__ void cluster_sync() {
 __host__ __device__ constexpr uint32_t sw128(uint32_t r, uint32_t c) {
     return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
 }
+// 64-byte swizzle: byte offset of 16-byte chunk `c` (0..3) of row `r` in a
+// tile of 64-byte rows (8-row groups 512 bytes apart).
+__host__ __device__ constexpr uint32_t sw64(uint32_t r, uint32_t c) {
+    return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
+}
 
 }  // namespace tc
 }  // namespace mla
@@ -247,6 +252,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int c
         "[%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
+}
+
+// ------------------------------------------------------------ cp.async (16 bytes, zero-filled beyond src_bytes)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------ register reallocation (whole warpgroup)
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------ conversions

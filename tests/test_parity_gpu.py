@@ -128,6 +128,33 @@ def test_sparse_decode_small_matches_oracle(case):
     U.assert_attn_close(o.cpu().numpy(), U.oracle_o_lat(x, list(range(B)), q_lat=q_gpu), "latent o")
 
 
+@pytest.mark.parametrize("growth", ["flat", "step", "ramp"])
+def test_many_blocks_per_unit_and_rescaled_maximum(growth):
+    # 80 sequences (one unit each: no split) x 640 selected keys = 10 key blocks
+    # per unit, more than the gather pipeline has stages.  "step" scales the
+    # cache rows of the second half of each selection by 3, "ramp" by
+    # 1 + 0.35 * block index: later blocks raise the running maximum, which
+    # forces the rescaling of the accumulated output.
+    B, S, K = 80, 700, 640
+    t = synth.make_inputs(synth.small_workload(B, [S] * B, k=K, K=K, S_cap=S), seed=31)
+    if growth != "flat":
+        for b in range(B):
+            sel = t["topk_idx"][b].long()
+            for j in range(K // 64):
+                f = (3.0 if j >= 5 else 1.0) if growth == "step" else 1.0 + 0.35 * j
+                rows = sel[64 * j: 64 * (j + 1)]
+                t["kv_cache"][b, rows] = (t["kv_cache"][b, rows].float() * f).to(torch.bfloat16)
+                t["pe_cache"][b, rows] = (t["pe_cache"][b, rows].float() * f).to(torch.bfloat16)
+    d = _dev(t)
+    step = mla.DecodeStep(B, K)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    step.check_status()
+    x = U.oracle_inputs(t)
+    bs = [0, 1, 39, 79]
+    U.assert_attn_close(out.cpu().numpy()[bs], U.oracle_out(x, bs), f"many blocks ({growth})")
+
+
 def test_padding_out_of_range_and_empty_rows():
     B, S = 3, 512
     t = synth.make_inputs(synth.small_workload(B, [512, 300, 200], k=100, K=160, S_cap=S), seed=5)
