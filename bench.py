@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -84,15 +85,17 @@ def replica_seed(rank: int, base: int = 0) -> int:
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of the bench GPU during the timed region."""
+    """nvidia-smi samples (100 ms) of the bench GPU; only samples taken
+    between mark_start() and mark_stop() (the timed region) are kept."""
 
-    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
         try:
             props = torch.cuda.get_device_properties(device_index)
             self.bus = f"{props.pci_bus_id:02X}:{props.pci_device_id:02X}."
@@ -104,33 +107,48 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-f", self.path],
+                                          "-lms", "100", "-f", self.path],
                                          stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.6)   # let the sampler come up before the timed region
         except Exception:
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
 
     def stop(self) -> dict | None:
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        import datetime
         rows = []
         try:
             for line in open(self.path):
                 f = [x.strip() for x in line.split(",")]
-                if len(f) >= 10:
-                    rows.append(f)
+                if len(f) < 11:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
+                    continue
+                rows.append(f[1:])
         finally:
             os.unlink(self.path)
         mine = [r for r in rows if self.bus and self.bus in r[1].upper()]
         if mine or len({r[0] for r in rows}) > 1:
             rows = mine
         if not rows:
-            return None
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
 
         def num(x):
             try:
@@ -154,18 +172,31 @@ def measured_peaks() -> dict:
         return {}
 
 
-def traffic_record(kernel_src: str) -> float | None:
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the kernel source as it is now."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_kernel_sparse_b64_ctx16384_top2048.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "sparse_latent_attention_decode_b300", "csrc", f)
+                  for f in ("attn.cu", "tc05.cuh", "common.cuh")]
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def traffic_record() -> float | None:
+    """DRAM bytes (read + write) per launch of the attention kernel, from the
+    committed ncu summary, if that summary was taken on the kernel sources as
+    they are now (its `kernel_source_sha256:` line); else None."""
     try:
-        rec = json.load(open(path))
-    except Exception:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
         return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    if rec.get("kernel_source_sha256") != sha:
+    sha = re.search(r"^kernel_source_sha256:\s*([0-9a-f]{64})", text, re.M)
+    val = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not sha or not val or sha.group(1) != kernel_source_digest():
         return None
-    return rec.get("dram_bytes_per_launch")
+    return float(val.group(1))
 
 
 def selected_rows(topk: torch.Tensor, end_pos: torch.Tensor) -> int:
@@ -174,17 +205,18 @@ def selected_rows(topk: torch.Tensor, end_pos: torch.Tensor) -> int:
 
 
 def oracle_sample(t: dict, wl, budget_s: float, max_seqs: int | None = None):
-    """Time the float64 oracle's full step on sequences 0, 1, ... until the
-    budget is used (at least one).  Returns (sequences, seconds)."""
+    """Time the float64 oracle's full step on sequences 0, 1, ... (cycling over
+    the batch) until the budget is used (at least one; at most max_seqs).
+    Returns (sequence-steps, seconds)."""
     from oracle import mla_oracle as O
     from sparse_latent_attention_decode_b300 import synth
     inv = O.yarn_inv_freq()
     scale = O.softmax_scale()
     wkv = synth.to_f64(t["wkv_b"])
     done, spent = 0, 0.0
-    limit = wl.B if max_seqs is None else min(wl.B, max_seqs)
-    while done < limit and (done == 0 or spent < budget_s):
-        b = done
+    limit = None if max_seqs is None else max_seqs
+    while (limit is None or done < limit) and (done == 0 or spent < budget_s):
+        b = done % wl.B
         x = {k: synth.to_f64(t[k][b:b + 1]) for k in ("q_nope", "q_pe", "kv_cache", "pe_cache", "topk_idx",
                                                      "end_pos")}
         t0 = time.perf_counter()
@@ -215,24 +247,22 @@ def run_ours(args):
     step = mla.DecodeStep(B, K, device=dev)
     args_dev = (d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
 
-    # ---- device-resident inputs
+    # ---- device-resident inputs: the timed steps (kernels chained by
+    # programmatic dependent launch, nothing recorded between them)
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         step(*args_dev)
     torch.cuda.synchronize()
     st = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    kt = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    for ev in kt:       # the library re-records these on the launching stream; a first record
-        ev.record()     # through torch marks them recorded for torch's elapsed_time()
     clocks = ClockSampler(local)
+    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
+    clocks.mark_start()
     t_wall = time.perf_counter()
     with mla.ProfileHook() as hook:
         for i in range(args.steps):
             flush.fill_((i + 7) & 0xFF)
-            hook.set_events(kt[2 * i], kt[2 * i + 1])
             st[2 * i].record()
             step(*args_dev)
             st[2 * i + 1].record()
@@ -240,13 +270,29 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
+    clocks.mark_stop()
     clk = clocks.stop()
     step.check_status()
     step_ms = [st[2 * i].elapsed_time(st[2 * i + 1]) for i in range(args.steps)]
-    kern_ms = [kt[2 * i].elapsed_time(kt[2 * i + 1]) for i in range(args.steps)]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, dev)
-    kern = statistics.mean(kern_ms)
+
+    # ---- the attention kernel alone: CUDA events recorded by the library on
+    # the launching stream right before and after it (these steps are not the
+    # timed ones: an event between two kernels separates them)
+    n_kern = min(args.steps, args.kernel_steps)
+    kt = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_kern)]
+    for ev in kt:       # the library re-records these on the launching stream; a first record
+        ev.record()     # through torch marks them recorded for torch's elapsed_time()
+    torch.cuda.synchronize()
+    with mla.ProfileHook() as khook:
+        for i in range(n_kern):
+            flush.fill_((i + 11) & 0xFF)
+            khook.set_events(kt[2 * i], kt[2 * i + 1])
+            step(*args_dev)
+    torch.cuda.synchronize()
+    step.check_status()
+    kern = statistics.mean(kt[2 * i].elapsed_time(kt[2 * i + 1]) for i in range(n_kern))
 
     # ---- end to end through the host-buffer API
     h = {k: t[k].pin_memory() for k in ("q_nope", "q_pe", "topk_idx", "end_pos")}
@@ -277,16 +323,15 @@ def run_ours(args):
     hbm = float(hbm) if hbm else FALLBACK_HBM_GBS
     alg_bytes = rows * ROW_BYTES
     achieved = alg_bytes / (kern * 1e-3) / 1e9
-    kernel_src = os.path.join(ROOT, "sparse_latent_attention_decode_b300", "csrc", "decode.cu")
-    traffic = traffic_record(kernel_src)
+    traffic = traffic_record()
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         n, secs = oracle_sample(t, wl, budget_s=args.cpu_budget)
         cpu = {"value": n / secs, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": f"sequences 0..{n - 1} of the {args.workload} batch ({n} of {B}); float64 numpy, "
-                         f"full step per sequence (RoPE, absorb, masked scores over all end_pos keys, softmax, "
-                         f"PV, up-projection); {secs:.1f} s"}
+               "sample": f"{n} sequence-steps of the {args.workload} batch (sequences taken in order, "
+                         f"cycling over the {B} of the batch); float64 numpy, full step per sequence (RoPE, "
+                         f"absorb, masked scores over all end_pos keys, softmax, PV, up-projection); {secs:.1f} s"}
 
     line = {
         "metric": METRIC, "value": world * B / (ms_max * 1e-3), "unit": UNIT, "n_gpus": world,
@@ -343,12 +388,15 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=4000,
+                    help="timed steps (long enough for several clock samples)")
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--kernel-steps", type=int, default=200,
+                    help="extra steps in which the attention kernel alone is timed")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps

@@ -178,8 +178,8 @@ int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, float *out, mla
  * the process exits).  The call allocates nothing.
  *   - Arguments, layouts and results are those of mla_sparse_decode.
  *   - Returns MLA_ERR_SIZE when mla_sparse_decode_workspace_size(B, K) is 0
- *     or exceeds MLA_STATIC_WS_BYTES (e.g. B*128*512*4 bytes of latent output
- *     alone must fit when wkv_b is given).
+ *     or exceeds MLA_STATIC_WS_BYTES (the bf16 latent output alone takes
+ *     B*128*512*2 bytes, so B <= 256).
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents

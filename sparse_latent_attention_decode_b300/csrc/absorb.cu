@@ -5,13 +5,14 @@
 // mla-decode (first einsum: q_nope . W_UK per head), and "Rotated query part"
 // page, excerpt apply-rope (pair rotation of q_pe).
 //
-// One CTA per head h computes, in the transposed ("swap-AB") form that puts
-// the 512 latent columns on the 128-row MMA dimension,
-//     q~_h^T [512, B] = W_UK[h]^T [512, 128] . q_nope_h^T [128, B]
-// as four M=128 tiles with N = the batch (up to 128 sequences per pass).
-// W_UK[h] (128 KB) is loaded once by TMA and read MN-major; the batch tile
-// arrives K-major through a 3-D tensor map over q_nope.  Results leave TMEM
-// as bf16 rows of q_lat.
+// One CTA per (latent tile t, head h) computes, in the transposed
+// ("swap-AB") form that puts 128 latent columns on the MMA rows,
+//     q~_h^T [128t .. 128t+127, B] = W_UK[h][:, tile]^T [128, 128] . q_nope_h^T [128, B]
+// with N = the batch (up to 128 sequences per pass): 512 CTAs of 128
+// threads.  The W_UK tile (32 KB) arrives by TMA and is read MN-major; the
+// batch tile arrives K-major through a 3-D tensor map over q_nope.  While the
+// copies are in flight, the CTA rotates pairs 8t .. 8t+7 of q_pe for every
+// sequence.  Results leave TMEM as bf16 rows of q_lat.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc05.cuh"
@@ -24,48 +25,87 @@ using namespace tc;
 constexpr int NMAX = 128;                      // sequences per pass
 constexpr int A_BOX = 128 * 128;               // one [128 d][64 c] box of W_UK, bytes
 constexpr int B_BOX = NMAX * 128;              // one [128 b][64 d] box of q_nope, bytes
-constexpr int SMEM_BYTES = 8 * A_BOX + 2 * B_BOX + 1024;
+constexpr int SMEM_BYTES = 2 * A_BOX + 2 * B_BOX + 1024;
+constexpr int PAIRS_PER_TILE = NPAIR / 4;      // rotary pairs handled by each latent tile
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
 struct Bars {
-    uint64_t a_full[4], b_full, mma_done;
+    uint64_t a_full, b_full, mma_done;
     uint32_t tmem_base;
 };
 
-__global__ void __launch_bounds__(128, 1)
+// Interleaved rotation of pairs [8t, 8t+8) of q_pe[b, h] for every sequence,
+// four items per thread at a time so that the loads overlap.
+__device__ __forceinline__ void rope_part(const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis,
+                                          int max_seq_len, const int32_t *__restrict__ end_pos, int B, int h,
+                                          int t, uint16_t *__restrict__ q_lat, int32_t *status, int tid) {
+    constexpr int BATCH = 4;
+    const int total = B * PAIRS_PER_TILE;
+    for (int k0 = tid; k0 < total; k0 += 128 * BATCH) {
+        int pos[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int k = k0 + 128 * u;
+            pos[u] = k < total ? end_pos[k / PAIRS_PER_TILE] - 1 : -1;
+        }
+        uint32_t w[BATCH];
+        float2 cs[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int k = k0 + 128 * u;
+            const int b = k / PAIRS_PER_TILE, i = PAIRS_PER_TILE * t + k % PAIRS_PER_TILE;
+            const bool in = k < total && pos[u] >= 0 && pos[u] < max_seq_len;
+            w[u] = in ? reinterpret_cast<const uint32_t *>(q_pe + ((size_t)b * H + h) * DR)[i] : 0u;
+            cs[u] = in ? cis[(size_t)pos[u] * NPAIR + i] : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int k = k0 + 128 * u;
+            if (k >= total) continue;
+            const int b = k / PAIRS_PER_TILE, i = PAIRS_PER_TILE * t + k % PAIRS_PER_TILE;
+            const float x0 = bflo(w[u]), x1 = bfhi(w[u]);
+            const uint32_t packed = uint32_t(f2bf(x0 * cs[u].x - x1 * cs[u].y)) |
+                                    (uint32_t(f2bf(x0 * cs[u].y + x1 * cs[u].x)) << 16);
+            reinterpret_cast<uint32_t *>(q_lat + ((size_t)b * H + h) * QL + C)[i] = packed;
+            if ((pos[u] < 0 || pos[u] >= max_seq_len) && i == 0 && h == 0) report(status, MLA_DEV_BAD_POSITION);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(128)
     absorb_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
                   const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis, int max_seq_len,
                   const int32_t *__restrict__ end_pos, int B, uint16_t *__restrict__ q_lat, int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem, *sB = smem + 8 * A_BOX;
-    const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t *sA = smem, *sB = smem + 2 * A_BOX;
+    const int t = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int t = 0; t < 4; ++t) mbar_init(&bars.a_full[t], 1);
+        mbar_init(&bars.a_full, 1);
         mbar_init(&bars.b_full, 1);
         mbar_init(&bars.mma_done, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&bars.tmem_base, 512);
+        tmem_alloc(&bars.tmem_base, NMAX);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the attention grid may be scheduled as soon as every CTA of this one has started
+    if (tid == 0) grid_dep_launch();
     const uint32_t tmem = bars.tmem_base;
     const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
     bool ok = true;
 
     if (tid == 0) {
-        // W_UK[h] = rows h*256 .. h*256+127 of wkv_b; tile t = latent columns 128t .. 128t+127
-        for (int t = 0; t < 4; ++t) {
-            mbar_expect_tx(&bars.a_full[t], 2 * A_BOX);
-            tma_load_2d(smem_u32(sA + (2 * t) * A_BOX), &wmap, 128 * t, h * WROWS, &bars.a_full[t]);
-            tma_load_2d(smem_u32(sA + (2 * t + 1) * A_BOX), &wmap, 128 * t + 64, h * WROWS, &bars.a_full[t]);
-        }
+        // W_UK[h] = rows h*256 .. h*256+127 of wkv_b; this tile = latent columns 128t .. 128t+127
+        mbar_expect_tx(&bars.a_full, 2 * A_BOX);
+        tma_load_2d(smem_u32(sA), &wmap, 128 * t, h * WROWS, &bars.a_full);
+        tma_load_2d(smem_u32(sA + A_BOX), &wmap, 128 * t + 64, h * WROWS, &bars.a_full);
     }
 
     const int npass = (B + NMAX - 1) / NMAX;
@@ -77,38 +117,39 @@ __global__ void __launch_bounds__(128, 1)
             mbar_expect_tx(&bars.b_full, 2 * B_BOX);
             tma_load_3d(smem_u32(sB), &qmap, 0, h, n0, &bars.b_full);
             tma_load_3d(smem_u32(sB + B_BOX), &qmap, 64, h, n0, &bars.b_full);
+        }
+        if (pass == 0) rope_part(q_pe, cis, max_seq_len, end_pos, B, h, t, q_lat, status, tid);
+        if (tid == 0) {
             bool good = wait_until(&bars.b_full, pass & 1, deadline);
-            const uint32_t idesc = idesc_bf16(128, N, true, false);
-            for (int t = 0; t < 4 && good; ++t) {
-                if (pass == 0) good = wait_until(&bars.a_full[t], 0, deadline);
-                if (!good) break;
+            if (pass == 0) good = good && wait_until(&bars.a_full, 0, deadline);
+            if (good) {
                 tc_fence_after();
+                const uint32_t idesc = idesc_bf16(128, N, true, false);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = smem_desc(smem_u32(sA + (2 * t) * A_BOX) + kk * 2048, A_BOX, 1024, 2);
+                    const uint64_t ad = smem_desc(smem_u32(sA) + kk * 2048, A_BOX, 1024, 2);
                     const uint64_t bd = smem_desc(smem_u32(sB + (kk >> 2) * B_BOX) + (kk & 3) * 32, 16, 1024, 2);
-                    mma_ss(tmem + t * NMAX, ad, bd, idesc, kk > 0);
+                    mma_ss(tmem, ad, bd, idesc, kk > 0);
                 }
+                mma_commit(&bars.mma_done);
+            } else {
+                report(status, MLA_DEV_TIMEOUT);
             }
-            if (good) mma_commit(&bars.mma_done);
-            else report(status, MLA_DEV_TIMEOUT);
         }
         ok = __syncthreads_and(wait_until(&bars.mma_done, pass & 1, deadline));
         if (!ok) break;
         tc_fence_after();
         // epilogue: lane = latent column within the tile, column = sequence
         const uint32_t trow = tmem + (uint32_t(32 * warp) << 16);
-        for (int t = 0; t < 4; ++t) {
-            for (int j0 = 0; j0 < N; j0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(trow + t * NMAX + j0, v);
-                tmem_ld_wait();
-                const int c = 128 * t + 32 * warp + lane;
+        const int c = 128 * t + 32 * warp + lane;
+        for (int j0 = 0; j0 < N; j0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(trow + j0, v);
+            tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int b = n0 + j0 + i;
-                    if (b < B) q_lat[((size_t)b * H + h) * QL + c] = f2bf(__uint_as_float(v[i]));
-                }
+            for (int i = 0; i < 16; ++i) {
+                const int b = n0 + j0 + i;
+                if (b < B) q_lat[((size_t)b * H + h) * QL + c] = f2bf(__uint_as_float(v[i]));
             }
         }
         tc_fence_before();
@@ -116,27 +157,11 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (!ok && tid == 0) report(status, MLA_DEV_TIMEOUT);
 
-    // fused RoPE of q_pe: thread = (pair, sequence)
-    for (int k = tid; k < B * NPAIR; k += 128) {
-        const int b = k / NPAIR, i = k % NPAIR;
-        const int pos = end_pos[b] - 1;
-        uint32_t packed = 0;
-        if (pos >= 0 && pos < max_seq_len) {
-            const uint32_t w = reinterpret_cast<const uint32_t *>(q_pe + ((size_t)b * H + h) * DR)[i];
-            const float x0 = bflo(w), x1 = bfhi(w);
-            const float2 cs = cis[(size_t)pos * NPAIR + i];
-            packed = uint32_t(f2bf(x0 * cs.x - x1 * cs.y)) | (uint32_t(f2bf(x0 * cs.y + x1 * cs.x)) << 16);
-        } else if (i == 0 && h == 0) {
-            report(status, MLA_DEV_BAD_POSITION);
-        }
-        reinterpret_cast<uint32_t *>(q_lat + ((size_t)b * H + h) * QL + C)[i] = packed;
-    }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, NMAX);
     }
 }
 
@@ -175,8 +200,8 @@ extern "C" int mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const 
             return MLA_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    absorb::absorb_kernel<<<H, 128, absorb::SMEM_BYTES, s>>>(wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis),
-                                                            max_seq_len, end_pos, B, q_lat, dev_status);
+    absorb::absorb_kernel<<<dim3(4, H), 128, absorb::SMEM_BYTES, s>>>(
+        wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, q_lat, dev_status);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

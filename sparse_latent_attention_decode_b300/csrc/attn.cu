@@ -1,5 +1,5 @@
 // Sparse latent attention on the 5th-generation tensor cores (tcgen05 + TMEM),
-// fed by 16-byte cp.async row gathers.
+// fed by 16-byte cp.async row gathers from eight warps.
 //
 // Source: DeepSeek-V3.2-Exp atlas, "Attention weights" page, excerpt
 // mla-decode: scores = (q~ . kv + q_pe . pe) * scale over the cached rows,
@@ -11,18 +11,49 @@
 //   CTA r gathers, for every selected key, latent columns [256r, 256r+256)
 //   and rotary columns [32r, 32r+32) -- each byte of a selected row is read
 //   from HBM exactly once by the pair.
-//   QK  : S_r[128 heads, 64 keys] = Q_r . K_r^T  (A = Q_r resident in TMEM,
-//         B = the gathered tile, K-major), 18 MMAs of K=16.
+//   QK  : S_r[128 heads, 64 keys] = Q_r . K_r^T, 16 MMAs of K=16 with the
+//         latent part of Q_r in TMEM and 2 with its rotary part in shared
+//         memory; B = the gathered tile, K-major.
 //   The two partial score tiles are exchanged through distributed shared
-//   memory (fp16, scaled to log2 units) and summed: both CTAs then hold the
-//   full scores and run the same online softmax (one thread per head).
+//   memory (raw scores as fp16, st.async into a ring of three receive
+//   buffers whose mbarriers count the arriving bytes) and summed: both CTAs
+//   then hold the full scores and run the same online softmax.
 //   PV  : O_r[128 heads, 256 latent] += P[128, 64] . V_r[64, 256]  (A = P
-//         in TMEM as bf16, B = the same gathered tile read MN-major).
-// TMEM per CTA: O_r 256 columns, Q_r 144, S 64, P 32 (512 allocated).
-// The softmax keeps a running maximum per head that is raised only when a
-// block's maximum exceeds it by more than 8 (log2 units); O and the running
-// sum are rescaled then, which keeps every exponent <= 2^8 and is exact up to
-// rounding because numerator and denominator share the same maximum.
+//         as bf16 in shared memory, B = the same gathered tile read MN-major).
+// TMEM per CTA: O_r columns [0,256), latent Q_r [256,384), two score
+// buffers S0 [384,448) and S1 [448,512).  A score buffer is released as soon
+// as the softmax has read it; P(j) is written (128-byte-swizzled, K-major)
+// over the peer's partial scores in receive slot j mod 3, row by row by the
+// thread that consumed that row.
+//
+// Warp roles (640 threads, five warpgroups):
+//   warps 0-7   gather: every thread copies 9 of a block's 2304 16-byte
+//               chunks with cp.async; the stage's mbarrier is signalled by
+//               the copies' completion (cp.async.mbarrier.arrive.noinc), so
+//               a block is published as soon as its own bytes have landed;
+//   warp 8      issues QK(j) once stage j is full and score buffer j%2 has
+//               been read (block j-2);
+//   warp 9      issues PV(j) once P(j) is in shared memory;
+//   warps 12-15 softmax of the even blocks, warps 16-19 of the odd blocks
+//               (ping-pong): one thread per head, all 64 keys of its block.
+// The selection of the unit is staged in shared memory once (positions
+// outside [0, end_pos) become -1), so no global index load sits on the
+// per-block path.
+//
+// Online softmax with a lazy running maximum m (log2 units): block j's
+// maximum replaces m only when it exceeds m by more than 8, which keeps
+// every exponent <= 2^8; numerator and denominator share m, so the result is
+// exact up to rounding.  m passes from the warpgroup of block j-1 to that of
+// block j through shared memory (one value per head); whichever warpgroup
+// raises m rescales O (after PV(j-1)), and each keeps its own running sum,
+// brought to the current m when it sees m change.
+//
+// Exchange ring without credits: block i is sent only after the peer's
+// block i-1 has been received here and PV(i-2) has finished reading P(i-2)
+// from slot (i-2) mod 3; the peer sends block i-1 only after it has consumed
+// block i-3 from the same slot (i mod 3) and PV(i-3) has read P(i-3) from
+// it.  The warpgroup that sends block i-1 is the one that received block
+// i-3, so that slot's previous mbarrier phase has completed too.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc05.cuh"
@@ -35,26 +66,26 @@ namespace attn {
 using namespace tc;
 
 constexpr int NK = 64;                       // keys per block
-constexpr int NS = 5;                        // gather pipeline stages
+constexpr int NS = 4;                        // gather pipeline stages
 constexpr int STAGE_KV = 4 * NK * 128;       // 4 atom columns of 64 latent x 64 keys (128B swizzle)
 constexpr int STAGE_PE = NK * 64;            // 32 rotary columns x 64 keys (64B swizzle)
 constexpr int STAGE = STAGE_KV + STAGE_PE;   // 36864
+constexpr int NRECV = 3;                     // exchange ring depth
 constexpr int RECV = H * NK * 2;             // fp16 partial scores of the peer, 128 x 64
-constexpr int SMEM_BYTES = NS * STAGE + 2 * RECV + 1024;
-constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 400, P_COL = 464, TMEM_COLS = 512;
-// warps 0..7 gather (cp.async), 8..11 softmax, 12 MMA, 13..15 idle: four
-// warpgroups, so that registers can move from the gather warps to the softmax
-constexpr int THREADS = 512;
-constexpr int GATHER_THREADS = 256;
-constexpr int CHUNKS = NK * 36;              // 16-byte chunks per stage: 32 latent + 4 rotary per key
-constexpr int CHUNKS_PER_THREAD = CHUNKS / GATHER_THREADS;   // 9
-constexpr int MMA_WARP = 12;
-// A gather thread publishes block j once it has issued block j+LAG and the
-// copies of block j have landed.  The MMA issues QK two blocks ahead of PV, so
-// block j+2 must be published without waiting for a stage that PV(j) frees:
-// (j + 2 + LAG) - NS < j, i.e. LAG <= NS - 3.
-constexpr int LAG = 2;
-static_assert(LAG <= NS - 3, "gather publication lag would deadlock against the QK lookahead");
+constexpr int IDX_CAP = 4096;                // selection entries of one unit staged in shared memory
+constexpr int QROPE = H * 64;                // rotary part of Q_r: 128 heads x 32 bf16 (64B swizzle)
+constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_CAP * 4 + 1024;
+constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 384, TMEM_COLS = 512;   // S buffer k at S_COL + 64 k
+constexpr int THREADS = 640;
+constexpr int GATHER_THREADS = 256;          // warps 0-7
+constexpr int CPT = NK * 36 / GATHER_THREADS;   // 9 chunks per gather thread per block
+static_assert(CPT * GATHER_THREADS == NK * 36, "chunks must divide evenly");
+constexpr int QK_WARP = 8, PV_WARP = 9;
+constexpr int SOFTMAX_WARP0 = 12;            // warps 12-19: two warpgroups
+constexpr int WG_THREADS = 128;
+// registers per thread after reallocation: 256*72 + 128*56 + 256*136 <= 640*96
+constexpr int REG_GATHER = 72, REG_MMA = 56, REG_SOFTMAX = 136;
+static_assert(256 * REG_GATHER + 128 * REG_MMA + 256 * REG_SOFTMAX <= THREADS * 96, "register split");
 constexpr float RESCALE_T = 8.f;             // lazy-max threshold (log2 units)
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
@@ -66,8 +97,9 @@ struct Params {
     const int32_t *end_pos;
     int S_cap, K, B;
     float scale_log2;   // softmax_scale * log2(e)
-    int n_split, split_len;
-    float *o_out;       // n_split == 1: normalised o, fp32 [B][128][512]
+    int n_split, split_len;   // split_len <= IDX_CAP
+    float *o_out;       // n_split == 1: normalised o, fp32 [B][128][512] (or NULL)
+    uint16_t *o_b16;    // n_split == 1: normalised o, bf16 [B][128][512] (or NULL)
     float *part_o;      // n_split > 1: per-split normalised o, fp32 [B*n_split][128][512]
     float *part_lse;    // n_split > 1: log2 of the split's softmax mass, [B*n_split][2][128]
     int32_t *status;
@@ -75,9 +107,13 @@ struct Params {
 
 struct Bars {
     uint64_t full[NS], empty[NS];
-    uint64_t s_full, s_free, p_full, pv_done, q_ready;
-    uint64_t recv_full[2], send_credit[2];
+    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_ready;
+    uint64_t recv_full[NRECV];
+    uint64_t m_ready[2];   // m after block j is in mval[j % 2]
+    uint64_t l_ready;      // both running sums are in lsum
     uint32_t tmem_base;
+    float mval[2][H];
+    float lsum[2][H];
 };
 
 __device__ __forceinline__ void fail(const Params &p) { report(p.status, MLA_DEV_TIMEOUT); }
@@ -86,9 +122,8 @@ __device__ __forceinline__ void fail(const Params &p) { report(p.status, MLA_DEV
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t deadline) {
     return __all_sync(0xffffffffu, wait_until(bar, parity, deadline));
 }
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t deadline) {
-    return __all_sync(0xffffffffu, wait_until_cluster(bar, parity, deadline));
-}
+
+__device__ __forceinline__ float max4(float a, float b, float c, float d) { return fmaxf(fmaxf(a, b), fmaxf(c, d)); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_kernel(Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -96,9 +131,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
     uint8_t *recv = smem + NS * STAGE;
+    uint8_t *qrope = recv + NRECV * RECV;
+    int32_t *sidx = reinterpret_cast<int32_t *>(qrope + QROPE);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t r = cluster_rank(), peer = r ^ 1u;
+    // Launched as a programmatic dependent of the preceding grid: nothing an
+    // earlier grid may have written (q_lat, the caches, the selection) is read
+    // before it has completed.
+    grid_dep_wait();
     const int unit = blockIdx.x >> 1;
     const int b = unit / p.n_split, split = unit % p.n_split;
     const int e = p.end_pos[b];
@@ -108,42 +149,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     const int nblk = (seq_ok && t1 > t0) ? (t1 - t0 + NK - 1) / NK : 0;
     if (!seq_ok && tid == 0 && r == 0 && split == 0) report(p.status, MLA_DEV_BAD_END_POS);
 
+    // the unit's selection, padded to whole blocks; padding and positions
+    // outside [0, end_pos) become -1
+    {
+        const int32_t *sel = p.topk + (size_t)b * p.K;
+        for (int i = tid; i < nblk * NK; i += THREADS) {
+            const int slot = t0 + i;
+            const int id = slot < t1 ? sel[slot] : -1;
+            sidx[i] = (id >= 0 && id < e) ? id : -1;
+        }
+    }
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bars.full[s], GATHER_THREADS), mbar_init(&bars.empty[s], 1);
-        mbar_init(&bars.s_full, 1);
-        mbar_init(&bars.s_free, 128);
-        mbar_init(&bars.p_full, 128);
-        mbar_init(&bars.pv_done, 1);
-        mbar_init(&bars.q_ready, 128);
-        for (int k = 0; k < 2; ++k) mbar_init(&bars.recv_full[k], 128), mbar_init(&bars.send_credit[k], 128);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&bars.s_full[k], 1);
+            mbar_init(&bars.s_free[k], WG_THREADS);
+            mbar_init(&bars.p_full[k], WG_THREADS);
+            mbar_init(&bars.pv_done[k], 1);
+            mbar_init(&bars.m_ready[k], WG_THREADS);
+        }
+        mbar_init(&bars.q_ready, 2 * WG_THREADS);
+        mbar_init(&bars.l_ready, 2 * WG_THREADS);
+        for (int k = 0; k < NRECV; ++k) mbar_init(&bars.recv_full[k], 1);
         fence_mbar_init();
     }
-    if (warp == MMA_WARP) {
+    if (warp == QK_WARP) {
         tmem_alloc(&bars.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
-    cluster_sync();   // barriers of both CTAs initialised, TMEM address published
+    cluster_sync();   // barriers of both CTAs initialised, TMEM address published, selection staged
     tc_fence_after();
+    // The dependent grid (value up-projection) may start its prologue now.
+    // This comes after grid_dep_wait, so every grid before this one has
+    // completed once a dependent of this grid runs.
+    if (tid == 0) grid_dep_launch();
     const uint32_t tmem = bars.tmem_base;
     const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
 
     if (warp < 8) {
         // ------------------------------------------------------------ gather producers
-        // 256 threads copy a stage's 2304 16-byte chunks with cp.async, 9 each.
-        // Chunk e = tid + 256 q belongs to key e / 36; chunks 0..31 of a key are
-        // its latent half (4 atom columns x 8, 128-byte swizzle), 32..35 its
-        // rotary half (64-byte swizzle).  Invalid keys are zero-filled.
-        regs_dec<96>();
-        uint32_t dst_off[CHUNKS_PER_THREAD];
-        int src_off[CHUNKS_PER_THREAD], key[CHUNKS_PER_THREAD];
-        bool is_pe[CHUNKS_PER_THREAD];
+        // Chunk ch = tid + 256 q (q < 9) of a block belongs to key ch / 36;
+        // chunks 0..31 of a key are its latent half (4 atom columns x 8,
+        // 128-byte swizzle), 32..35 its rotary half (64-byte swizzle).
+        // Unselected keys are zero-filled.
+        regs_dec<REG_GATHER>();
+        uint32_t dst_off[CPT];
+        int src_off[CPT], key[CPT];
+        uint32_t pe_mask = 0;
 #pragma unroll
-        for (int q = 0; q < CHUNKS_PER_THREAD; ++q) {
+        for (int q = 0; q < CPT; ++q) {
             const int ch = tid + GATHER_THREADS * q;
             key[q] = ch / 36;
             const int c = ch % 36;
-            is_pe[q] = c >= 32;
             if (c < 32) {
                 const int a = c >> 3, cc = c & 7;
                 dst_off[q] = a * (NK * 128) + sw128(key[q], cc);
@@ -152,116 +210,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 const int cc = c - 32;
                 dst_off[q] = STAGE_KV + sw64(key[q], cc);
                 src_off[q] = 32 * r + 8 * cc;
+                pe_mask |= 1u << q;
             }
         }
         const uint16_t *kvb = p.kv + (size_t)b * p.S_cap * C;
         const uint16_t *peb = p.pe + (size_t)b * p.S_cap * DR;
-        const int32_t *sel = p.topk + (size_t)b * p.K;
-        int cur[CHUNKS_PER_THREAD], nxt[CHUNKS_PER_THREAD];
-        auto load_idx = [&](int j, int(&dst)[CHUNKS_PER_THREAD]) {
-#pragma unroll
-            for (int q = 0; q < CHUNKS_PER_THREAD; ++q) {
-                const int slot = t0 + j * NK + key[q];
-                const int id = slot < t1 ? sel[slot] : -1;
-                dst[q] = (id >= 0 && id < e) ? id : -1;
-            }
-        };
-        if (nblk > 0) load_idx(0, nxt);
-        int j = 0;
-        for (; j < nblk; ++j) {
-#pragma unroll
-            for (int q = 0; q < CHUNKS_PER_THREAD; ++q) cur[q] = nxt[q];
-            if (j + 1 < nblk) load_idx(j + 1, nxt);   // prefetch: used next iteration
+        for (int j = 0; j < nblk; ++j) {
             const int s = j % NS;
             if (j >= NS && !warp_wait(&bars.empty[s], ((j / NS) - 1) & 1, deadline)) {
                 fail(p);
                 break;
             }
             const uint32_t base = smem_u32(stages + s * STAGE);
+            const int32_t *bidx = sidx + j * NK;
 #pragma unroll
-            for (int q = 0; q < CHUNKS_PER_THREAD; ++q) {
-                const int row = cur[q] < 0 ? 0 : cur[q];
-                const uint16_t *src = is_pe[q] ? peb + (size_t)row * DR + src_off[q] : kvb + (size_t)row * C + src_off[q];
-                cp_async16(base + dst_off[q], src, cur[q] < 0 ? 0u : 16u);
+            for (int q = 0; q < CPT; ++q) {
+                const int id = bidx[key[q]];
+                const size_t row = id < 0 ? 0 : (size_t)id;
+                const uint16_t *src = ((pe_mask >> q) & 1u) ? peb + row * DR + src_off[q] : kvb + row * C + src_off[q];
+                cp_async16(base + dst_off[q], src, id < 0 ? 0u : 16u);
             }
-            cp_async_commit();
-            if (j >= LAG) {   // the copies of block j-LAG have landed: publish them
-                cp_async_wait<LAG>();
-                fence_proxy_async_smem();
-                mbar_arrive(&bars.full[(j - LAG) % NS]);
-            }
+            // the stage's mbarrier counts this thread once its copies have landed
+            cp_async_arrive_noinc(&bars.full[s]);
         }
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        for (int jj = max(0, j - LAG); jj < j; ++jj) mbar_arrive(&bars.full[jj % NS]);
-    } else if (warp >= 12) {
-        // ------------------------------------------------------------ MMA issuer (warp 12, one thread)
-        regs_dec<64>();
-        if (warp == MMA_WARP && lane == 0 && nblk > 0) {
-            bool ok = wait_until(&bars.q_ready, 0, deadline);
-            tc_fence_after();
-            constexpr uint32_t idesc_qk = idesc_bf16(128, NK, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j % NS;
-                if (!wait_until(&bars.full[s], (j / NS) & 1, deadline)) return false;
-                if (j > 0 && !wait_until(&bars.s_free, (j - 1) & 1, deadline)) return false;
-                tc_fence_after();
-                const uint32_t base = smem_u32(stages + s * STAGE);
+        cp_async_wait<0>();   // no copy of this thread outlives the branch
+    } else if (warp < SOFTMAX_WARP0) {
+        // ------------------------------------------------------------ MMA issuers (warp 8: QK, warp 9: PV)
+        regs_dec<REG_MMA>();
+        if (lane == 0 && nblk > 0 && (warp == QK_WARP || warp == PV_WARP)) {
+            bool ok = true;
+            if (warp == QK_WARP) {
+                constexpr uint32_t idesc_qk = idesc_bf16(128, NK, false, false);
+                ok = wait_until(&bars.q_ready, 0, deadline);
+                const uint32_t qr = smem_u32(qrope);
+                for (int j = 0; ok && j < nblk; ++j) {
+                    const int s = j % NS, k = j & 1;
+                    // stage j gathered; score buffer k read by the softmax of block j-2
+                    ok = wait_until(&bars.full[s], (j / NS) & 1, deadline) &&
+                         (j < 2 || wait_until(&bars.s_free[k], ((j - 2) >> 1) & 1, deadline));
+                    if (!ok) break;
+                    // the stage was written by cp.async (generic proxy) and is read by the MMA (async proxy)
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const uint32_t base = smem_u32(stages + s * STAGE);
+                    const uint32_t sc = tmem + S_COL + 64 * k;
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    mma_ts(tmem + S_COL, tmem + Q_COL + kk * 8,
-                           smem_desc(base + (kk >> 2) * (NK * 128) + (kk & 3) * 32, 16, 1024, 2), idesc_qk, kk > 0);
+                    for (int kk = 0; kk < 16; ++kk)
+                        mma_ts(sc, tmem + Q_COL + kk * 8,
+                               smem_desc(base + (kk >> 2) * (NK * 128) + (kk & 3) * 32, 16, 1024, 2), idesc_qk, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_ts(tmem + S_COL, tmem + Q_COL + 128 + kk * 8, smem_desc(base + STAGE_KV + kk * 32, 16, 512, 4),
-                           idesc_qk, 1);
-                mma_commit(&bars.s_full);
-                return true;
-            };
-            auto issue_pv = [&](int j) -> bool {
-                const int s = j % NS;
-                if (!wait_until(&bars.p_full, j & 1, deadline)) return false;
-                tc_fence_after();
-                const uint32_t base = smem_u32(stages + s * STAGE);
+                    for (int kk = 0; kk < 2; ++kk)
+                        mma_ss(sc, smem_desc(qr + kk * 32, 16, 512, 4), smem_desc(base + STAGE_KV + kk * 32, 16, 512, 4),
+                               idesc_qk, 1);
+                    mma_commit(&bars.s_full[k]);
+                }
+            } else {
+                constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+                for (int j = 0; ok && j < nblk; ++j) {
+                    const int s = j % NS, k = j & 1;
+                    ok = wait_until(&bars.p_full[k], (j >> 1) & 1, deadline);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t base = smem_u32(stages + s * STAGE);
+                    const uint32_t pa = smem_u32(recv + (j % NRECV) * RECV);   // P(j), K-major, 128B swizzle
 #pragma unroll
-                for (int kk = 0; kk < NK / 16; ++kk)
-                    mma_ts(tmem + O_COL, tmem + P_COL + kk * 8, smem_desc(base + kk * 2048, NK * 128, 1024, 2),
-                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bars.pv_done);
-                mma_commit(&bars.empty[s]);
-                return true;
-            };
-            // QK runs two blocks ahead of PV: the softmax of block j overlaps QK(j+1)
-            ok = ok && issue_qk(0);
-            if (nblk > 1) ok = ok && issue_qk(1);
-            for (int j = 0; ok && j < nblk; ++j) {
-                if (j + 2 < nblk) ok = issue_qk(j + 2);
-                ok = ok && issue_pv(j);
+                    for (int kk = 0; kk < NK / 16; ++kk)
+                        mma_ss(tmem + O_COL, smem_desc(pa + kk * 32, 16, 1024, 2),
+                               smem_desc(base + kk * 2048, NK * 128, 1024, 2), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bars.pv_done[k]);
+                    mma_commit(&bars.empty[s]);
+                }
             }
             if (!ok) fail(p);
         }
     } else {
-        // ------------------------------------------------------------ softmax warps (one thread per head)
-        regs_inc<232>();
+        // ------------------------------------------------------------ softmax warpgroups (ping-pong)
+        // warpgroup w handles blocks j = w, w+2, ...; thread = head h, all 64 keys
+        regs_inc<REG_SOFTMAX>();
+        const int w = (warp - SOFTMAX_WARP0) >> 2;
         const int quad = warp & 3;
         const int h = 32 * quad + lane;
+        const int wtid = (warp - SOFTMAX_WARP0 - 4 * w) * 32 + lane;   // 0..127 within the warpgroup
         const uint32_t trow = tmem + (uint32_t(32 * quad) << 16);
         bool ok = true;
-        float m = -INFINITY, l = 0.f;
         if (nblk > 0) {
-            // Q_r -> TMEM: latent [256r, 256r+256) as 128 bf16 pairs, rotary [32r, 32r+32) as 16 pairs
+            // Q_r: latent [256r, 256r+256) -> TMEM as 128 bf16 pairs (warpgroup w
+            // stores 16-column groups 4w .. 4w+3); rotary [32r, 32r+32) -> shared
+            // memory, K-major with the 64-byte swizzle (warpgroup 1)
             const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + h) * QL);
-#pragma unroll
-            for (int c0 = 0; c0 < 9; ++c0) {
+            for (int c0 = 4 * w; c0 < 4 * w + 4; ++c0) {
                 uint32_t v[16];
-                const int src16 = c0 < 8 ? (256 * r) / 8 + c0 * 4 : (512 + 32 * r) / 8;  // in 16-byte units
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint4 w = qrow[src16 + q];
-                    v[4 * q] = w.x, v[4 * q + 1] = w.y, v[4 * q + 2] = w.z, v[4 * q + 3] = w.w;
+                    const uint4 x = qrow[(256 * r) / 8 + c0 * 4 + q];
+                    v[4 * q] = x.x, v[4 * q + 1] = x.y, v[4 * q + 2] = x.z, v[4 * q + 3] = x.w;
                 }
                 tmem_st16(trow + Q_COL + 16 * c0, v);
+            }
+            if (w == 1) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(qrope + sw64(h, c)) = qrow[(512 + 32 * r) / 8 + c];
+                fence_proxy_async_smem();
             }
             tmem_st_wait();
             tc_fence_before();
@@ -269,168 +319,200 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         }
         const uint32_t recv_local = smem_u32(recv);
         const uint32_t recv_peer = map_peer(recv_local, peer);
-        const int32_t *sel = p.topk + (size_t)b * p.K;
-        // Iteration j loads block j's partial scores and sends them to the peer,
-        // then finishes block j-1, whose peer half arrived during the previous
-        // iteration: the exchange latency hides behind a block of work.
-        float xp[NK];
-        uint32_t vpe = 0, vpo = 0;
-        for (int j = 0; j <= nblk && ok; ++j) {
-            float xc[NK];
-            uint32_t vce = 0, vco = 0;
-            if (j < nblk) {
-                // validity of the block's 64 keys (key k: bit k/2 of vce for even k, of vco for odd k)
-                const int slot = t0 + j * NK + 2 * lane;
-                const int i0 = slot < t1 ? sel[slot] : -1;
-                const int i1 = slot + 1 < t1 ? sel[slot + 1] : -1;
-                vce = __ballot_sync(0xffffffffu, i0 >= 0 && i0 < e);
-                vco = __ballot_sync(0xffffffffu, i1 >= 0 && i1 < e);
-
-                if (!warp_wait(&bars.s_full, j & 1, deadline)) { ok = false; break; }
-                tc_fence_after();
-                {
-                    uint32_t v[16];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld16(trow + S_COL + 16 * c, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) xc[16 * c + i] = __uint_as_float(v[i]) * p.scale_log2;
-                    }
-                }
+        const float sl2 = p.scale_log2;
+        float m_mine = -INFINITY;   // m after this warpgroup's previous block
+        float l = 0.f;              // this warpgroup's running sum, relative to m_mine
+        for (int j = w; j < nblk && ok; j += 2) {
+            const int k = j & 1;
+            const uint32_t sc = trow + S_COL + 64 * k;
+            // validity of the block's keys (bit i of vlo / vhi: key i / 32 + i)
+            const uint32_t vlo = __ballot_sync(0xffffffffu, sidx[j * NK + lane] >= 0);
+            const uint32_t vhi = __ballot_sync(0xffffffffu, sidx[j * NK + 32 + lane] >= 0);
+            if (!warp_wait(&bars.s_full[k], (j >> 1) & 1, deadline)) { ok = false; break; }
+            tc_fence_after();
+            float x[64];
+            {
+                uint32_t v0[16], v1[16], v2[16], v3[16];
+                tmem_ld16(sc, v0);
+                tmem_ld16(sc + 16, v1);
+                tmem_ld16(sc + 32, v2);
+                tmem_ld16(sc + 48, v3);
+                tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&bars.s_free);
-
-                // send my partial scores (fp16) into the peer's receive buffer j&1
-                const int kb = j & 1;
-                if (j >= 2 && !warp_wait_cluster(&bars.send_credit[kb], ((j >> 1) - 1) & 1, deadline)) {
-                    ok = false;
-                    break;
+                mbar_arrive(&bars.s_free[k]);   // QK(j+2) may overwrite the buffer
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    x[q] = __uint_as_float(v0[q]);
+                    x[16 + q] = __uint_as_float(v1[q]);
+                    x[32 + q] = __uint_as_float(v2[q]);
+                    x[48 + q] = __uint_as_float(v3[q]);
                 }
+            }
+            // ring credit: the peer's block j-1 has been received here (by the other
+            // warpgroup), and PV(j-2) has read P(j-2) from its slot
+            if (j >= 1 && !warp_wait(&bars.recv_full[(j - 1) % NRECV], ((j - 1) / NRECV) & 1, deadline)) {
+                ok = false;
+                break;
+            }
+            if (j >= 2 && !warp_wait(&bars.pv_done[k], ((j - 2) >> 1) & 1, deadline)) {
+                ok = false;
+                break;
+            }
+            {
+                const int kb = j % NRECV;
                 const uint32_t dst = recv_peer + kb * RECV + h * 128;
+                const uint32_t cbar = map_peer(smem_u32(&bars.recv_full[kb]), peer);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    st_cluster_v4(dst + ((c ^ (h & 7)) << 4), pack_f16_sat(xc[8 * c], xc[8 * c + 1]),
-                                  pack_f16_sat(xc[8 * c + 2], xc[8 * c + 3]), pack_f16_sat(xc[8 * c + 4], xc[8 * c + 5]),
-                                  pack_f16_sat(xc[8 * c + 6], xc[8 * c + 7]));
-                mbar_arrive_cluster(&bars.recv_full[kb], peer);
+                    st_async_v4(dst + ((c ^ (h & 7)) << 4), pack_f16_sat(x[8 * c], x[8 * c + 1]),
+                                pack_f16_sat(x[8 * c + 2], x[8 * c + 3]), pack_f16_sat(x[8 * c + 4], x[8 * c + 5]),
+                                pack_f16_sat(x[8 * c + 6], x[8 * c + 7]), cbar);
+                // receive the peer's half of block j: this warpgroup announces the bytes
+                if (wtid == 0) mbar_expect_tx(&bars.recv_full[kb], RECV);
+                if (!warp_wait(&bars.recv_full[kb], (j / NRECV) & 1, deadline)) { ok = false; break; }
+                const uint32_t src = recv_local + kb * RECV + h * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t a0, a1, a2, a3;
+                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                                 : "r"(src + ((c ^ (h & 7)) << 4)));
+                    const float2 f0 = unpack_f16(a0), f1 = unpack_f16(a1), f2 = unpack_f16(a2), f3 = unpack_f16(a3);
+                    x[8 * c] += f0.x, x[8 * c + 1] += f0.y, x[8 * c + 2] += f1.x, x[8 * c + 3] += f1.y;
+                    x[8 * c + 4] += f2.x, x[8 * c + 5] += f2.y, x[8 * c + 6] += f3.x, x[8 * c + 7] += f3.y;
+                }
             }
+            if ((vlo & vhi) != 0xffffffffu) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    x[q] = ((vlo >> q) & 1u) ? x[q] : -INFINITY;
+                    x[32 + q] = ((vhi >> q) & 1u) ? x[32 + q] : -INFINITY;
+                }
+            }
+            float bm;
+            {
+                float t[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) t[q] = max4(x[q], x[16 + q], x[32 + q], x[48 + q]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) t[q] = max4(t[q], t[4 + q], t[8 + q], t[12 + q]);
+                bm = max4(t[0], t[1], t[2], t[3]) * sl2;   // raw scores -> log2 units (scale > 0)
+            }
+            // running maximum: m after block j-1 comes from the other warpgroup
+            float m_prev = -INFINITY;
             if (j >= 1) {
-                const int jp = j - 1, kp = jp & 1;
-                if (!warp_wait_cluster(&bars.recv_full[kp], (jp >> 1) & 1, deadline)) { ok = false; break; }
-                {
-                    const uint32_t src = recv_local + kp * RECV + h * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t a0, a1, a2, a3;
-                        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                                     : "r"(src + ((c ^ (h & 7)) << 4)));
-                        const float2 f0 = unpack_f16(a0), f1 = unpack_f16(a1), f2 = unpack_f16(a2), f3 = unpack_f16(a3);
-                        xp[8 * c] += f0.x, xp[8 * c + 1] += f0.y, xp[8 * c + 2] += f1.x, xp[8 * c + 3] += f1.y;
-                        xp[8 * c + 4] += f2.x, xp[8 * c + 5] += f2.y, xp[8 * c + 6] += f3.x, xp[8 * c + 7] += f3.y;
-                    }
-                    mbar_arrive_cluster(&bars.send_credit[kp], peer);   // the peer may refill this buffer
-                }
-
-                // online softmax over block jp (lazy maximum)
-                float bm = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < NK; ++i) {
-                    const bool valid = ((i & 1) ? (vpo >> (i >> 1)) : (vpe >> (i >> 1))) & 1u;
-                    xp[i] = valid ? xp[i] : -INFINITY;
-                    bm = fmaxf(bm, xp[i]);
-                }
-                float f = 1.f;
-                if (bm > m + RESCALE_T) {
-                    f = ex2(m - bm);   // m = -inf -> 0
-                    m = bm;
-                }
-                uint32_t pk[NK / 2];
-                float sum = 0.f;
-#pragma unroll
-                for (int i = 0; i < NK; i += 2) {
-                    const float p0 = ex2(xp[i] - m), p1 = ex2(xp[i + 1] - m);   // -inf -> 0
-                    sum += p0 + p1;
-                    pk[i / 2] = pack_bf16(p0, p1);
-                }
-                if (m == -INFINITY) {   // nothing valid so far: P must be zero, not NaN
-                    sum = 0.f;
-#pragma unroll
-                    for (int i = 0; i < NK / 2; ++i) pk[i] = 0u;
-                }
-                l = l * f + sum;
-
-                // P and O are in use by PV(jp-1) until it completes
-                if (jp > 0) {
-                    if (!warp_wait(&bars.pv_done, (jp - 1) & 1, deadline)) { ok = false; break; }
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, f != 1.f)) {
-#pragma unroll 1
-                        for (int c0 = 0; c0 < 256; c0 += 16) {
-                            uint32_t v[16];
-                            tmem_ld16(trow + O_COL + c0, v);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                            tmem_st16(trow + O_COL + c0, v);
-                        }
-                    }
-                }
-                {
-                    uint32_t v[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = pk[i];
-                    tmem_st16(trow + P_COL, v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = pk[16 + i];
-                    tmem_st16(trow + P_COL + 16, v);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&bars.p_full);
+                if (!warp_wait(&bars.m_ready[(j - 1) & 1], ((j - 1) >> 1) & 1, deadline)) { ok = false; break; }
+                m_prev = bars.mval[(j - 1) & 1][h];
             }
+            const float m = bm > m_prev + RESCALE_T ? bm : m_prev;
+            bars.mval[k][h] = m;
+            mbar_arrive(&bars.m_ready[k]);
+            // bring this warpgroup's sum to m
+            if (m != m_mine) {
+                l = m_mine == -INFINITY ? 0.f : l * ex2(m_mine - m);
+                m_mine = m;
+            }
+            uint32_t pk[32];
+            float sum = 0.f;
+            if (m == -INFINITY) {   // nothing valid so far: P must be zero, not NaN
 #pragma unroll
-            for (int i = 0; i < NK; ++i) xp[i] = xc[i];
-            vpe = vce;
-            vpo = vco;
+                for (int q = 0; q < 32; ++q) pk[q] = 0u;
+            } else {
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < 64; q += 2) {
+                    const float p0 = ex2(fmaf(x[q], sl2, -m)), p1 = ex2(fmaf(x[q + 1], sl2, -m));   // -inf -> 0
+                    s4[(q >> 1) & 3] += p0 + p1;
+                    pk[q / 2] = pack_bf16(p0, p1);
+                }
+                sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            }
+            l += sum;
+            // raising m rescales O, after PV(j-1) has added its block
+            if (__any_sync(0xffffffffu, m != m_prev && m_prev != -INFINITY)) {
+                const float f = (m != m_prev && m_prev != -INFINITY) ? ex2(m_prev - m) : 1.f;
+                if (!warp_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, deadline)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c0 = 0; c0 < 256; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(trow + O_COL + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * f);
+                    tmem_st16(trow + O_COL + c0, v);
+                }
+            }
+            // P(j) over this thread's row of receive slot j mod 3 (same swizzle as
+            // the partial scores it replaces), then handed to the async proxy
+            {
+                const uint32_t prow = recv_local + (j % NRECV) * RECV + h * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((c ^ (h & 7)) << 4)),
+                                 "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                                 : "memory");
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars.p_full[k]);
         }
+
+        // ------------------------------------------------------------ final sums and epilogue
+        // m after the last block; both sums are brought to it and added
+        float m_fin = -INFINITY, lt = 0.f;
         if (ok && nblk > 0) {
-            if (!warp_wait(&bars.pv_done, (nblk - 1) & 1, deadline)) ok = false;
-            tc_fence_after();
+            const int jl = nblk - 1;
+            if (!warp_wait(&bars.m_ready[jl & 1], (jl >> 1) & 1, deadline)) ok = false;
+            if (ok) {
+                m_fin = bars.mval[jl & 1][h];
+                const float lw = (m_mine == -INFINITY || m_fin == -INFINITY) ? 0.f : l * ex2(m_mine - m_fin);
+                bars.lsum[w][h] = lw;
+                mbar_arrive(&bars.l_ready);
+                if (!warp_wait(&bars.l_ready, 0, deadline)) ok = false;
+                lt = bars.lsum[0][h] + bars.lsum[1][h];
+                if (ok && !warp_wait(&bars.pv_done[jl & 1], (jl >> 1) & 1, deadline)) ok = false;
+                tc_fence_after();
+            }
         }
         if (!ok) fail(p);
-
-        // ------------------------------------------------------------ epilogue
-        const bool have = ok && nblk > 0 && l > 0.f;
-        const float inv = have ? 1.f / l : 0.f;
-        float *dst = p.n_split == 1 ? p.o_out + ((size_t)b * H + h) * C + 256 * r
-                                    : p.part_o + ((size_t)unit * H + h) * C + 256 * r;
+        // warpgroup w normalises columns [128 w, 128 w + 128) of O_r
+        const bool have = ok && nblk > 0 && lt > 0.f;
+        const float inv = have ? 1.f / lt : 0.f;
+        const size_t orow = p.n_split == 1 ? ((size_t)b * H + h) * C : ((size_t)unit * H + h) * C;
+        const int col0 = 256 * r + 128 * w;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 256; c0 += 16) {
-            float4 o4[4];
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+            float o[16];
             if (have) {
                 uint32_t v[16];
-                tmem_ld16(trow + O_COL + c0, v);
+                tmem_ld16(trow + O_COL + 128 * w + c0, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    o4[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                        __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+                for (int q = 0; q < 16; ++q) o[q] = __uint_as_float(v[q]) * inv;
             } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) o4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q = 0; q < 16; ++q) o[q] = 0.f;
             }
+            if (p.n_split == 1 && p.o_b16) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o_b16 + orow + col0 + c0);
+                dst[0] = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+                                    pack_bf16(o[6], o[7]));
+                dst[1] = make_uint4(pack_bf16(o[8], o[9]), pack_bf16(o[10], o[11]), pack_bf16(o[12], o[13]),
+                                    pack_bf16(o[14], o[15]));
+            } else {
+                float4 *dst = reinterpret_cast<float4 *>((p.n_split == 1 ? p.o_out : p.part_o) + orow + col0 + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) reinterpret_cast<float4 *>(dst + c0)[q] = o4[q];
+                for (int q = 0; q < 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
         }
-        if (p.n_split > 1)
-            p.part_lse[((size_t)unit * 2 + r) * H + h] = have ? m + __log2f(l) : -INFINITY;
+        if (p.n_split > 1 && w == 0)
+            p.part_lse[((size_t)unit * 2 + r) * H + h] = have ? m_fin + __log2f(lt) : -INFINITY;
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == MMA_WARP) {
+    if (warp == QK_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -438,10 +520,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
 }
 
 // grid (B, H), 128 threads x 4 columns: merge the splits of one (sequence,
-// head); each latent half uses the masses its own CTA computed.
+// head); each latent half uses the masses its own CTA computed.  Writes the
+// normalised o as fp32 (o_out) or bf16 (o_b16), whichever is non-NULL.
 __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_lse, int n_split,
-                                                      float *__restrict__ o_out) {
+                                                      float *__restrict__ o_out, uint16_t *__restrict__ o_b16) {
+    grid_dep_wait();   // the partials come from the preceding attention grid
+    grid_dep_launch();
     const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x * 4, half = c >= 256 ? 1 : 0;
     float M = -INFINITY;
     for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_lse[(((size_t)b * n_split + s) * 2 + half) * H + h]);
@@ -460,8 +545,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    *reinterpret_cast<float4 *>(o_out + ((size_t)b * H + h) * C + c) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    const size_t o = ((size_t)b * H + h) * C + c;
+    if (o_b16)
+        *reinterpret_cast<uint2 *>(o_b16 + o) = make_uint2(pack_bf16(acc.x * inv, acc.y * inv),
+                                                           pack_bf16(acc.z * inv, acc.w * inv));
+    else
+        *reinterpret_cast<float4 *>(o_out + o) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 }  // namespace attn
@@ -472,6 +561,8 @@ int attn_n_split(int B, int K) {
     int n = B >= pairs ? 1 : pairs / B;
     const int max_split = (K + 127) / 128;
     if (n > max_split) n = max_split;
+    const int min_split = (K + attn::IDX_CAP - 1) / attn::IDX_CAP;   // a unit's selection fits in shared memory
+    if (n < min_split) n = min_split;
     return n < 1 ? 1 : n;
 }
 
@@ -488,8 +579,8 @@ size_t attn_workspace(int B, int K, int *n_split_out, int *split_len_out) {
 }
 
 int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, int S_cap, const int32_t *topk, int K,
-                const int32_t *end_pos, int B, float softmax_scale, float *o_out, void *ws, int32_t *status,
-                cudaStream_t s, int *launches) {
+                const int32_t *end_pos, int B, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
+                int32_t *status, cudaStream_t s, int *launches) {
     int n_split = 1, split_len = K;
     attn_workspace(B, K, &n_split, &split_len);
     attn::Params p{};
@@ -507,6 +598,7 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
     p.status = status;
     if (n_split == 1) {
         p.o_out = o_out;
+        p.o_b16 = o_b16;
     } else {
         const size_t units = (size_t)B * n_split;
         p.part_o = static_cast<float *>(ws);
@@ -523,14 +615,18 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
     }
     const ProfileHook &hook = profile_hook();
     const bool timed = hook.start && hook.stop;
+    // With the timing events in the stream the kernels are launched plainly:
+    // an event between two grids would separate them anyway.
     if (timed && cudaEventRecord(hook.start, s) != cudaSuccess) return MLA_ERR_CUDA;
-    attn::attn_kernel<<<2 * B * n_split, attn::THREADS, attn::SMEM_BYTES, s>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_k(!timed, attn::attn_kernel, dim3(2 * B * n_split), dim3(attn::THREADS), attn::SMEM_BYTES, s, p) !=
+        cudaSuccess)
+        return MLA_ERR_CUDA;
     if (timed && cudaEventRecord(hook.stop, s) != cudaSuccess) return MLA_ERR_CUDA;
     int n = 1;
     if (n_split > 1) {
-        attn::combine_kernel<<<dim3(B, H), 128, 0, s>>>(p.part_o, p.part_lse, n_split, o_out);
-        if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_k(!timed, attn::combine_kernel, dim3(B, H), dim3(128), 0, s, (const float *)p.part_o,
+                     (const float *)p.part_lse, n_split, o_out, o_b16) != cudaSuccess)
+            return MLA_ERR_CUDA;
         ++n;
     }
     if (launches) *launches += n;

@@ -19,7 +19,7 @@ static WsLayout ws_layout(int B, int K) {
     WsLayout w{};
     w.attn = 0;
     w.o_lat = align256(attn_workspace(B, K));
-    w.total = w.o_lat + align256((size_t)B * H * C * sizeof(float));
+    w.total = w.o_lat + align256((size_t)B * H * C * sizeof(uint16_t));   // bf16 o for the up-projection
     return w;
 }
 
@@ -46,13 +46,17 @@ extern "C" int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache
     if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     char *ws = static_cast<char *>(workspace);
-    float *o_lat = wkv_b ? reinterpret_cast<float *>(ws + L.o_lat) : out;
+    // with wkv_b the latent output stays internal, as bf16 (the up-projection
+    // rounds its operand to bf16 anyway); without it, o is the fp32 result
+    uint16_t *o_b16 = wkv_b ? reinterpret_cast<uint16_t *>(ws + L.o_lat) : nullptr;
     int launches = 0;
-    int rc = launch_attn(q_lat, kv_cache, pe_cache, S_cap, topk_idx, K, end_pos, B, softmax_scale, o_lat,
-                         ws + L.attn, dev_status, s, &launches);
+    int rc = launch_attn(q_lat, kv_cache, pe_cache, S_cap, topk_idx, K, end_pos, B, softmax_scale,
+                         wkv_b ? nullptr : out, o_b16, ws + L.attn, dev_status, s, &launches);
     count_launches(launches);
     if (rc != MLA_OK) return rc;
-    if (wkv_b) return launch_out_up(o_lat, wkv_b, B, out, dev_status, s);
+    const ProfileHook &hook = profile_hook();
+    const bool pdl = !(hook.start && hook.stop);
+    if (wkv_b) return launch_out_up(nullptr, o_b16, wkv_b, B, out, dev_status, s, pdl);
     return MLA_OK;
 }
 

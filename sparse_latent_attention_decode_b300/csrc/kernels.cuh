@@ -7,18 +7,44 @@
 
 namespace mla {
 
-int launch_out_up(const float *o_lat, const uint16_t *wkv_b, int B, float *out, int32_t *status, cudaStream_t s);
+// Value up-projection of the normalised latent output o, given either as
+// fp32 (o_f32, the standalone entry point) or as bf16 (o_b16, written by the
+// attention path); exactly one of them is non-NULL.
+int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
+                  int32_t *status, cudaStream_t s, bool pdl);
 
 // Sparse attention (tensor-core kernel + split combine).  Writes the
-// normalised latent output o [B][128][512] fp32 to o_out.  ws must hold
-// attn_workspace(B, K) bytes (256-byte aligned).
+// normalised latent output o [B][128][512] as fp32 to o_out or as bf16 to
+// o_b16 (exactly one non-NULL).  ws must hold attn_workspace(B, K) bytes
+// (256-byte aligned).
 size_t attn_workspace(int B, int K, int *n_split = nullptr, int *split_len = nullptr);
 int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, int S_cap, const int32_t *topk, int K,
-                const int32_t *end_pos, int B, float softmax_scale, float *o_out, void *ws, int32_t *status,
-                cudaStream_t s, int *launches);
+                const int32_t *end_pos, int B, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
+                int32_t *status, cudaStream_t s, int *launches);
+
+// Launch `kern` on stream s.  With pdl set, the launch allows programmatic
+// dependent launch: the grid may be scheduled while the preceding grid of the
+// stream is still running, and every kernel launched this way calls
+// griddepcontrol.wait before it reads anything an earlier grid may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // TMA tensor map of a bf16 tensor (dims[0] innermost); false on failure.
 bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                    const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
+                    const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle,
+                    CUtensorMapL2promotion promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
 }  // namespace mla

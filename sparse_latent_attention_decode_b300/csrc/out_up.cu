@@ -5,9 +5,16 @@
 //
 // One CTA per head h computes out_h^T [128 d, B] = W_UV[h] [128, 512] . o_h^T
 // [512, B] ("swap-AB": the head's 128 output features fill the MMA rows, the
-// batch is N).  W_UV[h] (128 KB) is loaded once by TMA (K-major); the latent
-// outputs o (fp32) are rounded to bf16 while they are written into the
-// 128-byte-swizzled operand tile, 64 sequences per pass.
+// batch is N), 64 sequences per pass.  W_UV[h] (128 KB) is loaded once by TMA
+// (K-major).  The latent outputs o arrive either as bf16 (written by the
+// attention kernel; loaded by TMA through a 3-D tensor map) or as fp32 (the
+// standalone entry point; rounded to bf16 while they are written into the
+// 128-byte-swizzled operand tile).
+//
+// The kernel is launched as a programmatic dependent of the attention grid.
+// It loads W_UV before griddepcontrol.wait: the attention grid itself waits
+// for every grid before it before it lets this one start, and it does not
+// write W_UV, so W_UV is final by then.  o is read only after the wait.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc05.cuh"
@@ -24,12 +31,44 @@ constexpr int SMEM_BYTES = 8 * A_BOX + 8 * B_ATOM + 1024;
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
 struct Bars {
-    uint64_t a_full, mma_done;
+    uint64_t a_full, b_full, mma_done;
     uint32_t tmem_base;
 };
 
+// fp32 o rows of one pass -> bf16 operand tile: 16-byte chunk (row, c/8), 64
+// chunks per row; loads are issued eight chunks at a time so that their
+// latencies overlap.
+__device__ __forceinline__ void stage_f32(const float *__restrict__ o_lat, int h, int n0, int nb, int N,
+                                          uint8_t *sB, int tid) {
+    constexpr int BATCH = 8;
+    const int total = N * 64;
+    for (int u0 = tid; u0 < total; u0 += 128 * BATCH) {
+        float4 x[BATCH][2];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const int u = u0 + 128 * k, row = u >> 6, ch = u & 63;
+            if (u < total && row < nb) {
+                const float4 *src = reinterpret_cast<const float4 *>(o_lat + ((size_t)(n0 + row) * H + h) * C + ch * 8);
+                x[k][0] = src[0];
+                x[k][1] = src[1];
+            } else {
+                x[k][0] = x[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const int u = u0 + 128 * k, row = u >> 6, ch = u & 63;
+            if (u < total)
+                *reinterpret_cast<uint4 *>(sB + (ch >> 3) * B_ATOM + sw128(row, ch & 7)) =
+                    make_uint4(pack_bf16(x[k][0].x, x[k][0].y), pack_bf16(x[k][0].z, x[k][0].w),
+                               pack_bf16(x[k][1].x, x[k][1].y), pack_bf16(x[k][1].z, x[k][1].w));
+        }
+    }
+}
+
 __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                        const float *__restrict__ o_lat, int B,
+                                                        const __grid_constant__ CUtensorMap omap,
+                                                        const float *__restrict__ o_f32, bool o_is_b16, int B,
                                                         float *__restrict__ out, int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
@@ -39,6 +78,7 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
 
     if (tid == 0) {
         mbar_init(&bars.a_full, 1);
+        mbar_init(&bars.b_full, 1);
         mbar_init(&bars.mma_done, 1);
         fence_mbar_init();
     }
@@ -57,6 +97,7 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
         for (int a = 0; a < 8; ++a)
             tma_load_2d(smem_u32(sA + a * A_BOX), &wmap, 64 * a, h * WROWS + DN, &bars.a_full);
     }
+    grid_dep_wait();   // o is written by the preceding grid
 
     bool ok = true;
     const int npass = (B + NMAX - 1) / NMAX;
@@ -64,22 +105,19 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
         const int n0 = pass * NMAX;
         const int nb = min(NMAX, B - n0);
         const int N = (nb + 15) & ~15;
-        // o rows of this pass -> bf16 operand tile: 16-byte chunk (row, c/8), 64 chunks per row
-        for (int u = tid; u < N * 64; u += 128) {
-            const int row = u >> 6, ch = u & 63;
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (row < nb) {
-                const float4 *src = reinterpret_cast<const float4 *>(o_lat + ((size_t)(n0 + row) * H + h) * C + ch * 8);
-                const float4 x0 = src[0], x1 = src[1];
-                w = make_uint4(pack_bf16(x0.x, x0.y), pack_bf16(x0.z, x0.w), pack_bf16(x1.x, x1.y),
-                               pack_bf16(x1.z, x1.w));
+        if (o_is_b16) {
+            if (tid == 0) {   // 8 boxes [64 b][64 c] of o_h; rows beyond B are zero-filled
+                mbar_expect_tx(&bars.b_full, 8 * B_ATOM);
+                for (int a = 0; a < 8; ++a) tma_load_3d(smem_u32(sB + a * B_ATOM), &omap, 64 * a, h, n0, &bars.b_full);
             }
-            *reinterpret_cast<uint4 *>(sB + (ch >> 3) * B_ATOM + sw128(row, ch & 7)) = w;
+        } else {
+            stage_f32(o_f32, h, n0, nb, N, sB, tid);
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            bool good = pass > 0 || wait_until(&bars.a_full, 0, deadline);
+            bool good = (pass > 0 || wait_until(&bars.a_full, 0, deadline)) &&
+                        (!o_is_b16 || wait_until(&bars.b_full, pass & 1, deadline));
             if (good) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16(128, N, false, false);
@@ -123,12 +161,23 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
 
 }  // namespace outup
 
-int launch_out_up(const float *o_lat, const uint16_t *wkv_b, int B, float *out, int32_t *status, cudaStream_t s) {
-    CUtensorMap wmap;
-    const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
-    const uint64_t strides[1] = {(uint64_t)C * 2};
-    const uint32_t box[2] = {64, 128};
-    if (!make_tmap_bf16(&wmap, wkv_b, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
+                  int32_t *status, cudaStream_t s, bool pdl) {
+    CUtensorMap wmap, omap;
+    {
+        const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
+        const uint64_t strides[1] = {(uint64_t)C * 2};
+        const uint32_t box[2] = {64, 128};
+        if (!make_tmap_bf16(&wmap, wkv_b, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+    }
+    if (o_b16) {
+        const uint64_t dims[3] = {(uint64_t)C, (uint64_t)H, (uint64_t)B};
+        const uint64_t strides[2] = {(uint64_t)C * 2, (uint64_t)H * C * 2};
+        const uint32_t box[3] = {64, 1, outup::NMAX};
+        if (!make_tmap_bf16(&omap, o_b16, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+    } else {
+        omap = wmap;   // unused
+    }
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
     static bool attr_set[64] = {};
@@ -138,9 +187,10 @@ int launch_out_up(const float *o_lat, const uint16_t *wkv_b, int B, float *out, 
             return MLA_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    outup::out_up_kernel<<<H, 128, outup::SMEM_BYTES, s>>>(wmap, o_lat, B, out, status);
+    const cudaError_t err = launch_k(pdl, outup::out_up_kernel, dim3(H), dim3(128), outup::SMEM_BYTES, s, wmap,
+                                     omap, o_f32, o_b16 != nullptr, B, out, status);
     count_launches(1);
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace mla
@@ -151,5 +201,5 @@ extern "C" int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, floa
     if (!o_lat || !wkv_b || !out) return MLA_ERR_NULL;
     if (!aligned16(o_lat) || !aligned16(wkv_b) || !aligned16(out)) return MLA_ERR_ALIGN;
     if (B < 1 || B > 4096) return MLA_ERR_SIZE;
-    return launch_out_up(o_lat, wkv_b, B, out, nullptr, (cudaStream_t)stream);
+    return launch_out_up(o_lat, nullptr, wkv_b, B, out, nullptr, (cudaStream_t)stream, false);
 }

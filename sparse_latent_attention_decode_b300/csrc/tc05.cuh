@@ -60,6 +60,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
+// Non-blocking probe: true when the phase with `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait: true when the phase with `parity` completed, false after
 // `limit` unsuccessful polls (each try_wait itself suspends for a while).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
@@ -258,11 +268,34 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int c
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// The mbarrier counts one arrival of this thread once all of its earlier
+// cp.async copies have completed (the arrival is not added to the expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+
+// ------------------------------------------------------------ asynchronous remote store (distributed shared memory)
+// 16 bytes into the shared memory of another CTA of the cluster; the bytes
+// are counted (complete_tx) on the mbarrier `cbar` of that same CTA.  Both
+// addresses are shared::cluster addresses (map_peer).
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+                     caddr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
+                 : "memory");
+}
+
+// ------------------------------------------------------------ programmatic dependent launch
+// Wait until the grids this one depends on have completed and their memory is visible.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the dependent grid to be scheduled (it still waits for this grid before reading its outputs).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------ register reallocation (whole warpgroup)
 template <int N>

@@ -25,7 +25,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // bf16 tensor of `rank` dims (dims[0] innermost, contiguous); strides_bytes
 // holds the byte strides of dims 1..rank-1.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                    const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle) {
+                    const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle,
+                    CUtensorMapL2promotion promotion) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t d[5];
@@ -38,7 +39,7 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t
         if (i > 0) s[i - 1] = strides_bytes[i - 1];
     }
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), d, s, b, e,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promotion,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
