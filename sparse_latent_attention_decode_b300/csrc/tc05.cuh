@@ -41,22 +41,25 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint64_t *bar, uint32_t cta)
         "r"(cta)
         : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread is parked (and issues
+// nothing) until the phase completes or about 0.5 ms have passed.
+constexpr uint32_t MBAR_SUSPEND_NS = 500000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(MBAR_SUSPEND_NS)
         : "memory");
     return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(MBAR_SUSPEND_NS)
         : "memory");
     return ok != 0;
 }
@@ -219,21 +222,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for the phase with `parity`; false once the global timer passes `deadline`.
+// Wait for the phase with `parity`; false once the global timer passes
+// `deadline`.  After a few polls the thread backs off with nanosleep, so that
+// waiting warps do not flood the shared-memory pipe with polls.
 __device__ __forceinline__ bool wait_until(uint64_t *bar, uint32_t parity, uint64_t deadline) {
-    for (;;) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() > deadline) return false;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i >= 2) __nanosleep(i < 8 ? 32 : 96);
+        if ((i & 31) == 31 && globaltimer_ns() > deadline) return false;
     }
 }
 __device__ __forceinline__ bool wait_until_cluster(uint64_t *bar, uint32_t parity, uint64_t deadline) {
-    for (;;) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (globaltimer_ns() > deadline) return false;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (i >= 2) __nanosleep(i < 8 ? 32 : 96);
+        if ((i & 31) == 31 && globaltimer_ns() > deadline) return false;
     }
 }
 
