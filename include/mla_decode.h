@@ -119,6 +119,22 @@ int rope_freqs_init(float *cis, const mla_rope_params *p, mla_stream_t stream);
 int mla_rope_apply(const mla_bf16 *q_pe, const float *cis, int max_seq_len, const int32_t *end_pos,
                    int B, float *q_pe_rot, int32_t *dev_status, mla_stream_t stream);
 
+/* mla_rope_apply_layout -- rotary embedding of 64-wide rotary vectors with a
+ * selectable pair layout ("Rotated query part" page, excerpt apply-rope, its
+ * `interleaved` argument), at position end_pos[b] - 1, in fp32:
+ *   interleaved = 1: pair i is (x[2i], x[2i+1]), rotated in place (the query
+ *                    layout; the same result as mla_rope_apply);
+ *   interleaved = 0: pair i is (x[i], x[i+32]); the real parts are written to
+ *                    features 0..31 and the imaginary parts to 32..63 (the
+ *                    layout the page's indexer uses).
+ *   x   [B][n_heads][64] bf16, device; out [B][n_heads][64] fp32, device, written
+ *       (zeros for a sequence whose position is outside the table:
+ *       MLA_DEV_BAD_POSITION).
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 65535,
+ * n_heads < 1 or > 1024, max_seq_len < 1, interleaved not 0 or 1). */
+int mla_rope_apply_layout(const mla_bf16 *x, const float *cis, int max_seq_len, const int32_t *end_pos, int B,
+                          int n_heads, int interleaved, float *out, int32_t *dev_status, mla_stream_t stream);
+
 /* mla_absorb_q -- the query of the latent attention: key absorption
  * ("Query content heads" page, excerpt mla-decode, first einsum) with the
  * RoPE of q_pe fused in:

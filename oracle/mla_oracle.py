@@ -113,6 +113,25 @@ def rope_interleaved(x: np.ndarray, cis: np.ndarray) -> np.ndarray:
     return out
 
 
+def rope_half_split(x: np.ndarray, cis: np.ndarray) -> np.ndarray:
+    """The indexer's layout (apply-rope with interleaved=False, Rotated query
+    part page): feature i and feature i + d/2 form the complex number
+    x[i] + j x[i + d/2], which is multiplied by cis[..., i]; the real parts are
+    written back to the first half and the imaginary parts to the second."""
+    d2 = x.shape[-1] // 2
+    z = x[..., :d2] + 1j * x[..., d2:]
+    y = z * cis
+    return np.concatenate([y.real, y.imag], axis=-1)
+
+
+def rope_for_positions(x: np.ndarray, end_pos: np.ndarray, inv_freq: np.ndarray, interleaved: bool = True):
+    """Rotate x [B, n_heads, 64] of each sequence at position end_pos[b] - 1, in
+    the interleaved (query) or half-split (indexer) layout."""
+    pos = np.asarray(end_pos, dtype=np.int64) - 1
+    cis = freqs_cis(pos, inv_freq)[:, None, :]
+    return rope_interleaved(x, cis) if interleaved else rope_half_split(x, cis)
+
+
 # --------------------------------------------------------------------------
 # softmax scale (Query heads page, excerpt mla-init)
 # --------------------------------------------------------------------------

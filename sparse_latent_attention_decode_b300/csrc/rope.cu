@@ -46,26 +46,32 @@ __global__ void rope_freqs_kernel(float2 *__restrict__ cis, RopeArgs a) {
     }
 }
 
-// One thread per (sequence, head, pair): rotate (x[2i], x[2i+1]) by
-// cis[end_pos[b]-1][i] in fp32.
-__global__ void rope_apply_kernel(const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis,
-                                  int max_seq_len, const int32_t *__restrict__ end_pos, int B,
-                                  float2 *__restrict__ out, int32_t *status) {
-    const long long n = (long long)B * H * NPAIR;
+// One thread per (sequence, head, pair): rotate pair i by cis[end_pos[b]-1][i]
+// in fp32.  Interleaved layout: the pair is (x[2i], x[2i+1]) and is written
+// back in place; half-split layout (the indexer's): the pair is (x[i], x[i+32])
+// and the real / imaginary parts go to slots i and i+32.
+__global__ void rope_apply_kernel(const uint16_t *__restrict__ x, const float2 *__restrict__ cis, int max_seq_len,
+                                  const int32_t *__restrict__ end_pos, int B, int n_heads, int interleaved,
+                                  float *__restrict__ out, int32_t *status) {
+    const long long n = (long long)B * n_heads * NPAIR;
     for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < n;
          k += (long long)gridDim.x * blockDim.x) {
         const int i = int(k % NPAIR);
-        const int b = int(k / (H * NPAIR));
+        const long long row = k / NPAIR;   // (b, head)
+        const int b = int(row / n_heads);
         const int pos = end_pos[b] - 1;
+        const uint16_t *xr = x + row * DR;
+        float *yr = out + row * DR;
+        const int s0 = interleaved ? 2 * i : i, s1 = interleaved ? 2 * i + 1 : i + NPAIR;
         if (pos < 0 || pos >= max_seq_len) {
-            out[k] = make_float2(0.f, 0.f);
-            if (i == 0 && (k / NPAIR) % H == 0) report(status, MLA_DEV_BAD_POSITION);
+            yr[s0] = 0.f, yr[s1] = 0.f;
+            if (i == 0 && row % n_heads == 0) report(status, MLA_DEV_BAD_POSITION);
             continue;
         }
-        const uint32_t w = reinterpret_cast<const uint32_t *>(q_pe)[k];
-        const float x0 = bflo(w), x1 = bfhi(w);
+        const float x0 = bf2f(xr[s0]), x1 = bf2f(xr[s1]);
         const float2 cs = cis[(long long)pos * NPAIR + i];
-        out[k] = make_float2(x0 * cs.x - x1 * cs.y, x0 * cs.y + x1 * cs.x);
+        yr[s0] = x0 * cs.x - x1 * cs.y;
+        yr[s1] = x0 * cs.y + x1 * cs.x;
     }
 }
 
@@ -112,19 +118,33 @@ extern "C" int rope_freqs_init(float *cis, const mla_rope_params *p, mla_stream_
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-extern "C" int mla_rope_apply(const mla_bf16 *q_pe, const float *cis, int max_seq_len, const int32_t *end_pos,
-                              int B, float *q_pe_rot, int32_t *dev_status, mla_stream_t stream) {
-    if (!q_pe || !cis || !end_pos || !q_pe_rot) return MLA_ERR_NULL;
-    if (!aligned16(q_pe) || !aligned16(cis) || !aligned16(q_pe_rot)) return MLA_ERR_ALIGN;
-    if (B < 1 || B > 65535 || max_seq_len < 1) return MLA_ERR_SIZE;
-    const long long n = (long long)B * H * NPAIR;
+static int rope_apply(const mla_bf16 *x, const float *cis, int max_seq_len, const int32_t *end_pos, int B,
+                      int n_heads, int interleaved, float *out, int32_t *dev_status, mla_stream_t stream) {
+    if (!x || !cis || !end_pos || !out) return MLA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(cis) || !aligned16(out)) return MLA_ERR_ALIGN;
+    if (B < 1 || B > 65535 || n_heads < 1 || n_heads > 1024 || max_seq_len < 1 ||
+        (interleaved != 0 && interleaved != 1))
+        return MLA_ERR_SIZE;
+    const long long n = (long long)B * n_heads * NPAIR;
     const int threads = 256;
-    const int blocks = int((n + threads - 1) / threads);
-    rope_apply_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(
-        q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B,
-        reinterpret_cast<float2 *>(q_pe_rot), dev_status);
+    const long long want = (n + threads - 1) / threads;
+    const int blocks = int(want < 148 * 32 ? want : 148 * 32);
+    rope_apply_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(x, reinterpret_cast<const float2 *>(cis),
+                                                                    max_seq_len, end_pos, B, n_heads, interleaved,
+                                                                    out, dev_status);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+extern "C" int mla_rope_apply(const mla_bf16 *q_pe, const float *cis, int max_seq_len, const int32_t *end_pos,
+                              int B, float *q_pe_rot, int32_t *dev_status, mla_stream_t stream) {
+    return rope_apply(q_pe, cis, max_seq_len, end_pos, B, H, 1, q_pe_rot, dev_status, stream);
+}
+
+extern "C" int mla_rope_apply_layout(const mla_bf16 *x, const float *cis, int max_seq_len, const int32_t *end_pos,
+                                     int B, int n_heads, int interleaved, float *out, int32_t *dev_status,
+                                     mla_stream_t stream) {
+    return rope_apply(x, cis, max_seq_len, end_pos, B, n_heads, interleaved, out, dev_status, stream);
 }
 
 namespace mla {

@@ -47,6 +47,7 @@ def _load():
         "mla_softmax_scale": (D, [ctypes.POINTER(RopeParams), I]),
         "rope_freqs_init": (I, [P, ctypes.POINTER(RopeParams), P]),
         "mla_rope_apply": (I, [P, P, I, P, I, P, P, P]),
+        "mla_rope_apply_layout": (I, [P, P, I, P, I, I, I, P, P, P]),
         "mla_absorb_q": (I, [P, P, P, I, P, P, I, P, P, P]),
         "mla_sparse_decode_workspace_size": (Z, [I, I]),
         "mla_sparse_decode": (I, [P, P, P, I, P, I, P, I, F, P, P, P, Z, P, P]),
@@ -64,7 +65,7 @@ def _load():
 
 _lib = _load()
 
-EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply",
+EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply", "mla_rope_apply_layout",
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
             "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws")
 STATIC_WS_BYTES = 32 << 20
@@ -136,6 +137,22 @@ def mla_rope_apply(q_pe, cis, end_pos, out=None, dev_status=None) -> torch.Tenso
     _need(out, "q_pe_rot", torch.float32, (B, N_HEADS, D_ROPE))
     _check(_lib.mla_rope_apply(_ptr(q_pe), _ptr(cis), cis.shape[0], _ptr(end_pos), B, _ptr(out),
                                _ptr(dev_status), _stream(q_pe.device)), "mla_rope_apply")
+    return out
+
+
+def mla_rope_apply_layout(x, cis, end_pos, interleaved: bool, out=None, dev_status=None) -> torch.Tensor:
+    """Rotary embedding of x [B, n_heads, 64] (bf16) at end_pos - 1, interleaved
+    pairs (query layout) or half-split pairs (indexer layout); fp32 result."""
+    B, n_heads = x.shape[0], x.shape[1]
+    _need(x, "x", torch.bfloat16, (B, n_heads, D_ROPE))
+    _need(cis, "cis", torch.float32)
+    _need(end_pos, "end_pos", torch.int32, (B,))
+    if out is None:
+        out = torch.empty(B, n_heads, D_ROPE, dtype=torch.float32, device=x.device)
+    _need(out, "out", torch.float32, (B, n_heads, D_ROPE))
+    _check(_lib.mla_rope_apply_layout(_ptr(x), _ptr(cis), cis.shape[0], _ptr(end_pos), B, n_heads,
+                                      1 if interleaved else 0, _ptr(out), _ptr(dev_status), _stream(x.device)),
+           "mla_rope_apply_layout")
     return out
 
 

@@ -33,10 +33,16 @@ def assert_attn_close(gpu, ora, what=""):
     return mx, mean
 
 
-def assert_rope_close(gpu, ora, x, what=""):
+def assert_rope_close(gpu, ora, x, what="", interleaved=True):
+    """Error of each rotated feature relative to the norm of the pair it
+    belongs to: (2i, 2i+1) interleaved, (i, i+32) half-split."""
     gpu = np.asarray(gpu, dtype=np.float64)
-    pair = np.hypot(x[..., 0::2], x[..., 1::2])
-    pair = np.repeat(pair, 2, axis=-1)
+    if interleaved:
+        pair = np.repeat(np.hypot(x[..., 0::2], x[..., 1::2]), 2, axis=-1)
+    else:
+        d2 = x.shape[-1] // 2
+        half = np.hypot(x[..., :d2], x[..., d2:])
+        pair = np.concatenate([half, half], axis=-1)
     err = np.abs(gpu - ora) / np.maximum(pair, 1e-30)
     assert err.max() <= ROPE_REL, f"{what}: rope rel err {err.max():.3e}"
     return err.max()

@@ -22,7 +22,7 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for want in ("rope_freqs_init", "mla_rope_apply", "mla_absorb_q", "mla_sparse_decode", "mla_out_up",
+    for want in ("rope_freqs_init", "mla_rope_apply", "mla_rope_apply_layout", "mla_absorb_q", "mla_sparse_decode", "mla_out_up",
                  "mla_sparse_decode_workspace_size", "mla_status_string"):
         assert want in names
 

@@ -307,3 +307,61 @@ def test_pins_catch_non_interleaved_pairing(monkeypatch):
     monkeypatch.setattr(O, "rope_interleaved", half_split)
     with pytest.raises(AssertionError):
         test_rope_unit_vector_lands_on_cos_sin_interleaved()
+
+
+# ------------------------------------------------- half-split (indexer) rotary layout
+def test_half_split_rope_unit_vectors():
+    # e_i (i < 32) becomes cos at slot i and sin at slot i + 32; e_(i+32) becomes
+    # -sin at slot i and cos at slot i + 32 (multiplication by exp(j theta))
+    f = O.yarn_inv_freq(**ROPE_KW)
+    t = 4095
+    cis = O.freqs_cis([t], f)[0]
+    for i in (0, 5, 10, 11, 23, 31):
+        th = t * f[i]
+        e = np.zeros(64)
+        e[i] = 1.0
+        y = O.rope_half_split(e, cis)
+        want = np.zeros(64)
+        want[i], want[i + 32] = math.cos(th), math.sin(th)
+        assert np.allclose(y, want, atol=1e-13)
+        e = np.zeros(64)
+        e[i + 32] = 1.0
+        y = O.rope_half_split(e, cis)
+        want = np.zeros(64)
+        want[i], want[i + 32] = -math.sin(th), math.cos(th)
+        assert np.allclose(y, want, atol=1e-13)
+
+
+def test_half_split_rope_is_the_interleaved_rotation_of_the_regrouped_pairs():
+    # moving feature i + 32 next to feature i turns the half-split layout into the
+    # interleaved one; the rotation must commute with that regrouping
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 64, 64))
+    f = O.yarn_inv_freq(**ROPE_KW)
+    cis = O.freqs_cis(np.arange(5) * 1000 + 7, f)[:, None, :]
+    inter = np.empty_like(x)
+    inter[..., 0::2], inter[..., 1::2] = x[..., :32], x[..., 32:]
+    y_int = O.rope_interleaved(inter, cis)
+    back = np.concatenate([y_int[..., 0::2], y_int[..., 1::2]], axis=-1)
+    assert np.allclose(O.rope_half_split(x, cis), back, atol=1e-12)
+    # pair norms (x[i], x[i+32]) are preserved, position 0 is the identity
+    y = O.rope_half_split(x, cis)
+    assert np.allclose(np.hypot(y[..., :32], y[..., 32:]), np.hypot(x[..., :32], x[..., 32:]), atol=1e-12)
+    assert np.allclose(O.rope_half_split(x, O.freqs_cis([0], f)[0]), x, atol=1e-15)
+
+
+def test_rope_for_positions_selects_the_layout():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 64, 64))
+    end = np.array([1, 2049, 16384])
+    f = O.yarn_inv_freq(**ROPE_KW)
+    cis = O.freqs_cis(end - 1, f)[:, None, :]
+    assert np.array_equal(O.rope_for_positions(x, end, f, interleaved=True), O.rope_interleaved(x, cis))
+    assert np.array_equal(O.rope_for_positions(x, end, f, interleaved=False), O.rope_half_split(x, cis))
+    assert np.array_equal(O.rope_for_positions(x, end, f), O.rope_for_batch(x, end, f))
+
+
+def test_pins_catch_interleaved_pairing_in_the_half_split_layout(monkeypatch):
+    monkeypatch.setattr(O, "rope_half_split", O.rope_interleaved)
+    with pytest.raises(AssertionError):
+        test_half_split_rope_unit_vectors()

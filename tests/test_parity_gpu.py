@@ -72,6 +72,53 @@ def test_rope_apply_reports_bad_position():
     assert torch.all(out == 0)
 
 
+@pytest.mark.parametrize("n_heads", [1, 64, 128])
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_rope_apply_layout_matches_oracle(n_heads, interleaved):
+    g = torch.Generator().manual_seed(17 + n_heads)
+    end = torch.tensor([1, 2, 333, 4097, 12000, 16384, 7], dtype=torch.int32)
+    x = torch.randn(7, n_heads, 64, generator=g).to(torch.bfloat16)
+    cis = mla.rope_freqs_init()
+    got = mla.mla_rope_apply_layout(x.cuda(), cis, end.cuda(), interleaved).cpu().double().numpy()
+    xd = synth.to_f64(x)
+    ora = O.rope_for_positions(xd, end.numpy(), U.INV_FREQ, interleaved=interleaved)
+    U.assert_rope_close(got, ora, xd, f"rope layout {interleaved}", interleaved=interleaved)
+
+
+def test_rope_apply_layout_interleaved_equals_query_rope():
+    g = torch.Generator().manual_seed(5)
+    end = torch.tensor([3, 16000], dtype=torch.int32, device="cuda")
+    x = torch.randn(2, 128, 64, generator=g).to(torch.bfloat16).cuda()
+    cis = mla.rope_freqs_init()
+    a = mla.mla_rope_apply_layout(x, cis, end, True)
+    b = mla.mla_rope_apply(x, cis, end)
+    assert torch.equal(a, b)
+
+
+def test_rope_apply_layout_reports_bad_position():
+    cis = mla.rope_freqs_init()
+    x = torch.ones(2, 64, 64, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mla.mla_rope_apply_layout(x, cis, torch.tensor([16385, 5], dtype=torch.int32, device="cuda"), False,
+                                    dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & mla.MLA_DEV_BAD_POSITION
+    assert torch.all(out[0] == 0) and torch.any(out[1] != 0)
+
+
+def test_rope_apply_layout_rejects_bad_arguments():
+    cis = mla.rope_freqs_init()
+    x = torch.ones(1, 64, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(1, 64, 64, dtype=torch.float32, device="cuda")
+    end = torch.ones(1, dtype=torch.int32, device="cuda")
+    st = mla._lib.mla_rope_apply_layout(mla._ptr(x), mla._ptr(cis), cis.shape[0], mla._ptr(end), 1, 64, 2,
+                                        mla._ptr(out), None, mla._stream(x.device))
+    assert st != 0
+    st = mla._lib.mla_rope_apply_layout(mla._ptr(x), mla._ptr(cis), cis.shape[0], mla._ptr(end), 1, 0, 1,
+                                        mla._ptr(out), None, mla._stream(x.device))
+    assert st != 0
+
+
 # ----------------------------------------------------------------- absorb / up-projection
 @pytest.mark.parametrize("B", [1, 3, 64, 130])
 def test_absorb_matches_oracle(B):
