@@ -228,6 +228,51 @@ def oracle_sample(t: dict, wl, budget_s: float, max_seqs: int | None = None):
 
 
 # ----------------------------------------------------------------- our arm
+def time_single_kernel(fn, n: int, flush) -> float:
+    """Mean device time (ms) of fn(), which enqueues one library kernel on the
+    current stream, with L2 flushed before each launch."""
+    for i in range(3):
+        flush.fill_(i)
+        fn()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        flush.fill_((i + 5) & 0xFF)
+        ev[2 * i].record()
+        fn()
+        ev[2 * i + 1].record()
+    torch.cuda.synchronize()
+    return statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n))
+
+
+def measure_next_rows(mla, synth, dev, flush, seed: int, n: int = 50) -> dict:
+    """The entry points beyond the decode step, each on its own workload:
+    algorithmic bytes per launch and the event-timed launch duration."""
+    out = {}
+    # half-split RoPE of an indexer-shaped query: 64 sequences x 64 heads x 64
+    B, nh = 64, 64
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(B, nh, 64, generator=g).to(torch.bfloat16).to(dev)
+    end = torch.randint(1, 16385, (B,), generator=g, dtype=torch.int32).to(dev)
+    cis = mla.rope_freqs_init(device=dev)
+    y = torch.empty(B, nh, 64, dtype=torch.float32, device=dev)
+    ms = time_single_kernel(lambda: mla.mla_rope_apply_layout(x, cis, end, False, out=y), n, flush)
+    nbytes = B * nh * 64 * (2 + 4) + B * 32 * 8 + B * 4
+    out["rope_half_split"] = {"workload": f"B={B} x {nh} heads x 64, end_pos uniform in [1, 16384]",
+                              "kernel_ms": ms, "alg_bytes_per_launch": nbytes,
+                              "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
+    # fp8 wkv_b dequantisation: 32768 x 512 e4m3 codes, 128 x 128 tiles
+    codes, scale = synth.make_fp8_weight(seed)
+    codes, scale = codes.to(dev), scale.to(dev)
+    w = torch.empty(codes.shape, dtype=torch.bfloat16, device=dev)
+    ms = time_single_kernel(lambda: mla.mla_weight_dequant_fp8(codes, scale, out=w), n, flush)
+    nbytes = codes.numel() * 3 + scale.numel() * 4
+    out["weight_dequant_fp8"] = {"workload": "wkv_b 32768 x 512 e4m3, fp32 scale per 128 x 128 tile",
+                                 "kernel_ms": ms, "alg_bytes_per_launch": nbytes,
+                                 "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
+    return out
+
+
 def run_ours(args):
     from sparse_latent_attention_decode_b300 import mla, synth
 
@@ -314,6 +359,8 @@ def run_ours(args):
     e2e_ms = max_over_ranks(statistics.mean(et[2 * i].elapsed_time(et[2 * i + 1]) for i in range(args.steps)),
                             world, dev)
 
+    next_rows = measure_next_rows(mla, synth, dev, flush, args.seed)
+
     if rank != 0:
         return None
 
@@ -350,6 +397,7 @@ def run_ours(args):
                      "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
                      "alg_bytes_per_launch": alg_bytes, "kernel_ms": kern},
         "cpu_baseline": cpu,
+        "next_rows": {k: dict(v, frac=v["achieved_gbs"] / hbm) for k, v in next_rows.items()},
         "clocks": clk,
         "gpu_launches": launches,
         "wall_s_timed_region": wall,

@@ -184,6 +184,25 @@ int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla
  * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096). */
 int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, float *out, mla_stream_t stream);
 
+/* mla_weight_dequant_fp8 -- block-scaled fp8 weight to bf16 (the pages'
+ * weight_dequant(wkv_b.weight, wkv_b.scale), "Rotated query part" page,
+ * excerpt mla-decode, run once and kept as the wkv_b of the absorbed path):
+ *   out[r][c] = bf16_rn( fp32( e4m3(w[r][c]) * scale[r / block][c / block] ) )
+ * The pages name the call but not its format; this entry reads it as OCP
+ * FP8 E4M3 codes (bias 7, no infinities, S.1111.111 = NaN) with one fp32
+ * multiplier per block x block tile (block 128 for DeepSeek-V3 checkpoints).
+ *   w     [rows][cols] uint8 e4m3 codes, device.
+ *   scale [ceil(rows/block)][ceil(cols/block)] fp32, device, 4-byte aligned.
+ *   out   [rows][cols] bf16, device, 2-byte aligned, written.  A NaN code
+ *         gives a NaN.
+ * Any rows, cols and block >= 1; when cols and block are multiples of 16 and
+ * w and out are 16-byte aligned the kernel moves 16 elements per access.
+ * For wkv_b: rows 32768, cols 512, block 128, scale [256][4].
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (rows, cols or block < 1,
+ * rows*cols > 2^40), MLA_ERR_CUDA. */
+int mla_weight_dequant_fp8(const uint8_t *w, const float *scale, int rows, int cols, int block, mla_bf16 *out,
+                           mla_stream_t stream);
+
 /* mla_sparse_decode_static_ws -- mla_sparse_decode without a caller-supplied
  * workspace.  The pages have no counterpart to this call; it exists for
  * callers that cannot allocate device memory (a plugin host that owns every

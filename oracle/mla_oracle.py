@@ -51,6 +51,60 @@ D_QK = D_NOPE + D_ROPE  # 192
 
 
 # --------------------------------------------------------------------------
+# fp8 weights: e4m3 decoding and block dequantisation ("Rotated query part"
+# page, excerpt mla-decode: weight_dequant(wkv_b.weight, wkv_b.scale), called
+# once and kept as the wkv_b of the absorbed path).  The pages name the call
+# only; the format is read as OCP FP8 E4M3 (sign, 4 exponent bits with bias 7,
+# 3 mantissa bits, no infinities, S.1111.111 = NaN) with one multiplier per
+# block x block tile.
+# --------------------------------------------------------------------------
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each 8-bit E4M3 code, from the format's definition:
+    exponent field 0 -> (-1)^s * m/8 * 2^-6 (subnormal); S.1111.111 -> NaN;
+    otherwise (-1)^s * (1 + m/8) * 2^(e-7)."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = (m / 8.0) * 2.0 ** -6
+    v = sign * np.where(e == 0, sub, normal)
+    return np.where((c & 0x7F) == 0x7F, np.nan, v)
+
+
+def dequant_block_fp8(codes, scale, block: int = 128) -> np.ndarray:
+    """Exact dequantised weight: e4m3(codes[r, c]) * scale[r // block, c // block]
+    in float64 (the product of a 4-bit and a 24-bit significand is exact)."""
+    codes = np.asarray(codes)
+    rows, cols = codes.shape
+    s = np.asarray(scale, dtype=np.float64)
+    assert s.shape == (-(-rows // block), -(-cols // block))
+    s_full = np.repeat(np.repeat(s, block, axis=0), block, axis=1)[:rows, :cols]
+    return e4m3_decode(codes) * s_full
+
+
+def round_to_bf16(x) -> np.ndarray:
+    """Round to the nearest bfloat16 (8 significant bits), ties to even, for
+    values in the normal range; NaN stays NaN."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                  # x = m * 2^e, 0.5 <= |m| < 1
+    r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)   # np.rint: ties to even
+    return np.where(np.isfinite(x), r, x)
+
+
+def dequant_to_bf16(codes, scale, block: int = 128) -> np.ndarray:
+    """The bf16 weight the decode consumes.  The rounding decides a bit
+    pattern, so it is taken in the precision of the library's dequantisation:
+    the code times the multiplier rounded to float32, then to bf16."""
+    codes = np.asarray(codes)
+    rows, cols = codes.shape
+    s = np.asarray(scale, dtype=np.float32)
+    s_full = np.repeat(np.repeat(s, block, axis=0), block, axis=1)[:rows, :cols]
+    p32 = e4m3_decode(codes).astype(np.float32) * s_full      # IEEE float32 product
+    return round_to_bf16(p32.astype(np.float64))
+
+
+# --------------------------------------------------------------------------
 # a1: frequency table (Transformer blocks page, excerpts rope + model-args)
 # --------------------------------------------------------------------------
 def yarn_correction_dim(num_rotations: float, dim: int, base: float, original_seq_len: int) -> float:

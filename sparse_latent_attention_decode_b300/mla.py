@@ -55,6 +55,7 @@ def _load():
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_profile_hook": (I, [P, P, P]),
         "mla_sparse_decode_static_ws": (I, [P, P, P, I, P, I, P, I, F, P, P, P, P]),
+        "mla_weight_dequant_fp8": (I, [P, P, I, I, I, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -67,7 +68,7 @@ _lib = _load()
 
 EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply", "mla_rope_apply_layout",
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
-            "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws")
+            "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws", "mla_weight_dequant_fp8")
 STATIC_WS_BYTES = 32 << 20
 
 
@@ -168,6 +169,22 @@ def mla_absorb_q(q_nope, q_pe, cis, end_pos, wkv_b, out=None, dev_status=None) -
     _need(out, "q_lat", torch.bfloat16, (B, N_HEADS, Q_LAT))
     _check(_lib.mla_absorb_q(_ptr(q_nope), _ptr(q_pe), _ptr(cis), cis.shape[0], _ptr(end_pos), _ptr(wkv_b), B,
                              _ptr(out), _ptr(dev_status), _stream(q_nope.device)), "mla_absorb_q")
+    return out
+
+
+def mla_weight_dequant_fp8(w, scale, block: int = 128, out=None) -> torch.Tensor:
+    """bf16 [rows, cols] from e4m3 codes w [rows, cols] (uint8 or float8_e4m3fn)
+    and fp32 block multipliers scale [ceil(rows/block), ceil(cols/block)]."""
+    if isinstance(w, torch.Tensor) and w.dtype == torch.float8_e4m3fn:
+        w = w.view(torch.uint8)
+    rows, cols = w.shape
+    _need(w, "w", torch.uint8, (rows, cols))
+    _need(scale, "scale", torch.float32, ((rows + block - 1) // block, (cols + block - 1) // block))
+    if out is None:
+        out = torch.empty(rows, cols, dtype=torch.bfloat16, device=w.device)
+    _need(out, "out", torch.bfloat16, (rows, cols))
+    _check(_lib.mla_weight_dequant_fp8(_ptr(w), _ptr(scale), rows, cols, block, _ptr(out), _stream(w.device)),
+           "mla_weight_dequant_fp8")
     return out
 
 

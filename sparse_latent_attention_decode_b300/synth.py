@@ -149,6 +149,25 @@ def make_inputs(wl: Workload, seed: int = 0, fill_tail: bool = False, threads: i
                 topk_idx=topk, end_pos=end_pos)
 
 
+def make_fp8_weight(seed: int, rows: int = N_HEADS * (D_NOPE + D_V), cols: int = KV_LORA, block: int = 128,
+                    name: str = "wkv_b_fp8"):
+    """A block-scaled fp8 weight: e4m3 codes [rows, cols] (uint8) and fp32
+    multipliers [ceil(rows/block), ceil(cols/block)].
+
+    Codes are N(0, 112) draws clamped to the e4m3 range +-448 and rounded to
+    e4m3 by torch's cast (so every tile spans most of the code range, as a
+    per-tile absmax quantisation leaves it); multipliers are
+    4 * 512^-0.5 / 448 * exp(N(0, 0.25^2)) per tile, so that the dequantised
+    weight has about the spread of the bf16 wkv_b.  No code is NaN."""
+    g = _gen(seed, name)
+    x = torch.randn(rows, cols, generator=g, dtype=torch.float32).mul_(112.0).clamp_(-448.0, 448.0)
+    codes = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    sr, sc = -(-rows // block), -(-cols // block)
+    z = torch.randn(sr, sc, generator=_gen(seed, name + "/scale"), dtype=torch.float32)
+    scale = torch.exp(z * 0.25) * (4.0 * KV_LORA ** -0.5 / 448.0)
+    return codes.contiguous(), scale.to(torch.float32).contiguous()
+
+
 def small_workload(B: int, end_pos, k=None, K=None, S_cap: int = 1024, selection: str = "uniform",
                    name: str = "small") -> Workload:
     """A reduced workload with the same distributions, for tests."""

@@ -8,6 +8,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 from oracle import mla_oracle as O
 from sparse_latent_attention_decode_b300 import synth
@@ -365,3 +366,64 @@ def test_pins_catch_interleaved_pairing_in_the_half_split_layout(monkeypatch):
     monkeypatch.setattr(O, "rope_half_split", O.rope_interleaved)
     with pytest.raises(AssertionError):
         test_half_split_rope_unit_vectors()
+
+
+# ----------------------------------------------------------------- fp8 weights
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256)
+    got = O.e4m3_decode(codes)
+    ref = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    # sign of zero
+    assert np.signbit(got[0x80]) and not np.signbit(got[0x00])
+
+
+def test_e4m3_decode_closed_form_codes():
+    # values fixed by the format: bias 7, 3 mantissa bits, no infinities
+    want = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 / 8 * 2.0 ** -6, 0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125,
+            0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0, 0xB8: -1.0, 0x30: 0.5}
+    got = O.e4m3_decode(list(want))
+    assert np.array_equal(got, np.array(list(want.values())))
+    assert np.isnan(O.e4m3_decode([0x7F, 0xFF])).all()
+
+
+def test_dequant_block_maps_tiles_to_their_multiplier():
+    # ragged 200 x 300 with block 128: a 2 x 3 grid of distinct powers of two
+    scale = np.array([[1.0, 2.0, 4.0], [8.0, 16.0, 32.0]])
+    codes = np.full((200, 300), 0x38)            # every code is 1.0
+    w = O.dequant_block_fp8(codes, scale, block=128)
+    for r, c in [(0, 0), (127, 127), (128, 0), (0, 128), (199, 299), (127, 256), (128, 255)]:
+        assert w[r, c] == scale[r // 128, c // 128]
+    codes = np.full((4, 6), 0xC0)                # -2.0, block 2: grid 2 x 3
+    w = O.dequant_block_fp8(codes, np.arange(1, 7, dtype=np.float64).reshape(2, 3), block=2)
+    assert np.array_equal(w, -2.0 * np.repeat(np.repeat(np.arange(1, 7).reshape(2, 3), 2, 0), 2, 1))
+
+
+def test_round_to_bf16_matches_torch_and_breaks_ties_to_even():
+    x = np.random.default_rng(1).standard_normal(50000).astype(np.float32) * 3.0
+    ref = torch.tensor(x).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.round_to_bf16(x.astype(np.float64)), ref)
+    ulp = 2.0 ** -7
+    assert O.round_to_bf16(1 + ulp / 2) == 1.0                 # tie, 1.0 is even
+    assert O.round_to_bf16(1 + 3 * ulp / 2) == 1 + 2 * ulp     # tie, rounds up to even
+    assert O.round_to_bf16(-(1 + 3 * ulp / 2)) == -(1 + 2 * ulp)
+    assert O.round_to_bf16(2 - ulp / 4) == 2.0                 # carries into the next binade
+
+
+def test_dequant_to_bf16_is_within_the_rounding_bound_of_the_exact_product():
+    codes, scale = synth.make_fp8_weight(3, rows=300, cols=260, block=128)
+    exact = O.dequant_block_fp8(codes.numpy(), scale.numpy().astype(np.float64), block=128)
+    b16 = O.dequant_to_bf16(codes.numpy(), scale.numpy(), block=128)
+    # half a bf16 ulp (2^-8 relative at most) plus the float32 rounding before it
+    assert np.all(np.abs(b16 - exact) <= (2.0 ** -8 + 2.0 ** -23) * np.abs(exact))
+    # every result is a bf16 value
+    assert np.array_equal(b16, O.round_to_bf16(b16))
+
+
+def test_fp8_synth_weight_spans_the_code_range():
+    codes, scale = synth.make_fp8_weight(0, rows=256, cols=512)
+    v = O.e4m3_decode(codes.numpy())
+    assert not np.isnan(v).any()
+    assert np.abs(v).max() == 448.0 and (np.abs(v) < 2.0 ** -6).any()     # saturated and subnormal codes
+    assert scale.shape == (2, 4) and (scale > 0).all()

@@ -298,3 +298,57 @@ def test_named_workload_matches_oracle_on_sampled_sequences(name):
         bs = sorted({int(ep.argmin()), int(ep.argmax()), wl.B // 2})
     x = _oracle_view(t)
     U.assert_attn_close(got[bs], U.oracle_out(x, bs), name)
+
+
+# ----------------------------------------------------------------- fp8 wkv_b
+def _assert_bits_equal(got_bf16, want_f64):
+    got = got_bf16.cpu().to(torch.float64).numpy()
+    nan = np.isnan(want_f64)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want_f64[~nan])
+    # the sign of zero is part of the bit pattern
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want_f64[~nan]))
+
+
+def test_dequant_wkv_b_is_bit_exact():
+    codes, scale = synth.make_fp8_weight(21)
+    got = mla.mla_weight_dequant_fp8(codes.cuda(), scale.cuda())
+    _assert_bits_equal(got, O.dequant_to_bf16(codes.numpy(), scale.numpy(), 128))
+
+
+@pytest.mark.parametrize("rows,cols,block", [(200, 300, 128), (130, 528, 128), (64, 96, 64), (7, 33, 1),
+                                             (1, 16, 128), (257, 512, 32), (3, 5, 4)])
+def test_dequant_ragged_shapes_and_blocks(rows, cols, block):
+    codes, scale = synth.make_fp8_weight(rows * 7 + cols, rows=rows, cols=cols, block=block, name="ragged")
+    got = mla.mla_weight_dequant_fp8(codes.cuda(), scale.cuda(), block=block)
+    _assert_bits_equal(got, O.dequant_to_bf16(codes.numpy(), scale.numpy(), block))
+
+
+def test_dequant_every_code_including_nan_and_signed_zero():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).reshape(16, 16)
+    scale = torch.tensor([[0.75]], dtype=torch.float32)
+    got = mla.mla_weight_dequant_fp8(codes.cuda(), scale.cuda(), block=16)
+    _assert_bits_equal(got, O.dequant_to_bf16(codes.numpy(), scale.numpy(), 16))
+
+
+def test_dequant_unaligned_output_takes_the_scalar_path():
+    codes, scale = synth.make_fp8_weight(4, rows=40, cols=128, block=128)
+    buf = torch.empty(40 * 128 + 1, dtype=torch.bfloat16, device="cuda")
+    out = buf[1:].view(40, 128)                   # 2-byte offset: not 16-byte aligned
+    mla.mla_weight_dequant_fp8(codes.cuda(), scale.cuda(), out=out)
+    _assert_bits_equal(out, O.dequant_to_bf16(codes.numpy(), scale.numpy(), 128))
+
+
+def test_decode_with_fp8_wkv_b_matches_oracle():
+    B = 3
+    t = synth.make_inputs(synth.small_workload(B, [700, 64, 1001], k=256, K=256, S_cap=1024), seed=29)
+    codes, scale = synth.make_fp8_weight(29)
+    d = _dev(t)
+    d["wkv_b"] = mla.mla_weight_dequant_fp8(codes.cuda(), scale.cuda())
+    step = mla.DecodeStep(B, 256)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    step.check_status()
+    x = U.oracle_inputs(t)
+    x["wkv_b"] = O.dequant_to_bf16(codes.numpy(), scale.numpy(), 128)
+    U.assert_attn_close(out.cpu().numpy(), U.oracle_out(x, list(range(B))), "decode with fp8 wkv_b")
