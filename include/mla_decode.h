@@ -184,6 +184,32 @@ int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla
  * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096). */
 int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, float *out, mla_stream_t stream);
 
+/* mla_cache_append -- write T new tokens per sequence into the caches ("Query
+ * heads" page, excerpt mla-init: the joint down-projection wkv_a emits the
+ * 512 latent features and the 64-wide shared rotary key; kv_norm is an
+ * RMSNorm over the latent; "Attention weights" page, excerpt mla-decode:
+ * kv_cache / pe_cache are read up to end_pos).  The pages do not print the
+ * write; the plain reading is: token s of sequence b sits at position
+ * pos = end_pos[b] - T + s, and
+ *   kv_cache[b][pos][:] = bf16( x * w / sqrt(mean(x^2) + eps) ),  x = kv_a[b][s][0:512]
+ *   pe_cache[b][pos][:] = bf16( rope_interleaved(kv_a[b][s][512:576], pos) )
+ * with fp32 arithmetic (the rotation as in mla_rope_apply).
+ *   kv_a      [B][T][576] bf16, device: the wkv_a output of the new tokens.
+ *   kv_norm_w [512] fp32, device (a bf16 weight widens exactly).
+ *   eps       RMSNorm epsilon (>= 0; 1e-6 in DeepSeek-V3 checkpoints).
+ *   cis       rotary table [max_seq_len][32][2] fp32 (rope_freqs_init).
+ *   end_pos   [B] int32: cached tokens of sequence b AFTER the append.
+ *   kv_cache  [B][S_cap][512] bf16, pe_cache [B][S_cap][64] bf16, device:
+ *             rows end_pos[b]-T .. end_pos[b]-1 are written, nothing else.
+ * A sequence with end_pos[b] < T or > S_cap is skipped (MLA_DEV_BAD_END_POS);
+ * a token whose position is outside the rotary table is skipped
+ * (MLA_DEV_BAD_POSITION).
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B, T, S_cap or
+ * max_seq_len < 1, B*T >= 2^31, eps negative or NaN). */
+int mla_cache_append(const mla_bf16 *kv_a, const float *kv_norm_w, float eps, const float *cis, int max_seq_len,
+                     const int32_t *end_pos, int B, int T, mla_bf16 *kv_cache, mla_bf16 *pe_cache, int S_cap,
+                     int32_t *dev_status, mla_stream_t stream);
+
 /* mla_weight_dequant_fp8 -- block-scaled fp8 weight to bf16 (the pages'
  * weight_dequant(wkv_b.weight, wkv_b.scale), "Rotated query part" page,
  * excerpt mla-decode, run once and kept as the wkv_b of the absorbed path):

@@ -304,6 +304,30 @@ def decode_step(q_nope, q_pe, kv_cache, pe_cache, wkv_b, topk_idx, end_pos, inv_
 
 
 # --------------------------------------------------------------------------
+# Cache append ("Query heads" page, excerpt mla-init and its prose: wkv_a
+# emits the 512 latent features and the 64-wide rotary key, kv_norm is an
+# RMSNorm of the latent; "Attention weights" page, excerpt mla-decode: the
+# caches are read up to end_pos).  The write itself is not printed; token s of
+# T new tokens sits at position end_pos - T + s.  RMSNorm is taken in its
+# standard form x * w / sqrt(mean(x^2) + eps) (its body is not on the pages).
+# --------------------------------------------------------------------------
+def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    return x * np.asarray(w, dtype=np.float64) / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def cache_rows(kv_a: np.ndarray, kv_norm_w: np.ndarray, eps: float, end_pos, inv_freq: np.ndarray):
+    """The rows the append writes: (positions [B, T], latent rows [B, T, 512],
+    rotary rows [B, T, 64]), unrounded float64."""
+    B, T = kv_a.shape[0], kv_a.shape[1]
+    pos = np.asarray(end_pos, dtype=np.int64)[:, None] - T + np.arange(T)[None, :]
+    latent = rms_norm(kv_a[..., :KV_LORA], kv_norm_w, eps)
+    cis = freqs_cis(pos.reshape(-1), inv_freq).reshape(B, T, -1)
+    rot = rope_interleaved(kv_a[..., KV_LORA:], cis)
+    return pos, latent, rot
+
+
+# --------------------------------------------------------------------------
 # independent formulations used only to pin the oracle
 # --------------------------------------------------------------------------
 def naive_attention_one(q_nope_b, q_pe_rot_b, kv, pe, wkv_b, topk_row, end_pos, scale):

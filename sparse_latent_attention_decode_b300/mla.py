@@ -56,6 +56,7 @@ def _load():
         "mla_profile_hook": (I, [P, P, P]),
         "mla_sparse_decode_static_ws": (I, [P, P, P, I, P, I, P, I, F, P, P, P, P]),
         "mla_weight_dequant_fp8": (I, [P, P, I, I, I, P, P]),
+        "mla_cache_append": (I, [P, P, F, P, I, P, I, I, P, P, I, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -68,7 +69,8 @@ _lib = _load()
 
 EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply", "mla_rope_apply_layout",
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
-            "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws", "mla_weight_dequant_fp8")
+            "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws", "mla_weight_dequant_fp8",
+            "mla_cache_append")
 STATIC_WS_BYTES = 32 << 20
 
 
@@ -188,6 +190,25 @@ def mla_weight_dequant_fp8(w, scale, block: int = 128, out=None) -> torch.Tensor
     return out
 
 
+def mla_cache_append(kv_a, kv_norm_w, cis, end_pos, kv_cache, pe_cache, eps: float = 1e-6,
+                     dev_status=None) -> None:
+    """Write the T new tokens of each sequence (kv_a [B, T, 576] bf16, the wkv_a
+    output) into kv_cache [B, S_cap, 512] / pe_cache [B, S_cap, 64] at
+    positions end_pos - T .. end_pos - 1: RMSNorm of the latent, rotation of
+    the rotary key."""
+    B, T = kv_a.shape[0], kv_a.shape[1]
+    S_cap = kv_cache.shape[1]
+    _need(kv_a, "kv_a", torch.bfloat16, (B, T, Q_LAT))
+    _need(kv_norm_w, "kv_norm_w", torch.float32, (KV_LORA,))
+    _need(cis, "cis", torch.float32)
+    _need(end_pos, "end_pos", torch.int32, (B,))
+    _need(kv_cache, "kv_cache", torch.bfloat16, (B, S_cap, KV_LORA))
+    _need(pe_cache, "pe_cache", torch.bfloat16, (B, S_cap, D_ROPE))
+    _check(_lib.mla_cache_append(_ptr(kv_a), _ptr(kv_norm_w), float(eps), _ptr(cis), cis.shape[0], _ptr(end_pos),
+                                 B, T, _ptr(kv_cache), _ptr(pe_cache), S_cap, _ptr(dev_status),
+                                 _stream(kv_a.device)), "mla_cache_append")
+
+
 def workspace_size(B: int, K: int) -> int:
     n = int(_lib.mla_sparse_decode_workspace_size(B, K))
     if n == 0:
@@ -285,6 +306,33 @@ class ProfileHook:
     @property
     def launches(self) -> int:
         return int(self.count.value)
+
+
+class CapturedStep:
+    """A callable captured once into a CUDA graph and then replayed: one graph
+    launch per step instead of one host call per kernel, so that the host never
+    paces the device.  Every tensor the callable touches must stay allocated
+    (the graph holds their addresses); ``out`` is what the captured call
+    returned, refreshed by each replay.  The library kernels keep their
+    programmatic-dependent-launch chaining inside the graph."""
+
+    def __init__(self, fn, *args, warmup: int = 2):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn(*args)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with ProfileHook() as hook:
+            with torch.cuda.graph(self.graph):
+                self.out = fn(*args)
+        self.kernels_per_replay = hook.launches
+
+    def __call__(self):
+        self.graph.replay()
+        return self.out
 
 
 class DecodeStep:

@@ -427,3 +427,53 @@ def test_fp8_synth_weight_spans_the_code_range():
     assert not np.isnan(v).any()
     assert np.abs(v).max() == 448.0 and (np.abs(v) < 2.0 ** -6).any()     # saturated and subnormal codes
     assert scale.shape == (2, 4) and (scale > 0).all()
+
+
+# ----------------------------------------------------------------- cache append
+U_INV_FREQ = O.yarn_inv_freq()
+
+def test_rms_norm_worked_values_and_invariants():
+    got = O.rms_norm(np.array([3.0, 4.0]), np.array([1.0, 2.0]), 0.0)
+    # mean of squares 12.5: 3 / sqrt(12.5) and 2 * 4 / sqrt(12.5)
+    assert np.allclose(got, [0.848528137423857, 2.262741699796952], rtol=0, atol=1e-15)
+    x = np.random.default_rng(2).standard_normal((5, 512))
+    y = O.rms_norm(x, np.ones(512), 0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, rtol=0, atol=1e-13)        # unit RMS
+    assert np.allclose(O.rms_norm(7.5 * x, np.ones(512), 0.0), y, rtol=1e-14)  # scale invariance
+    assert np.array_equal(O.rms_norm(np.zeros(512), np.ones(512), 1e-6), np.zeros(512))
+    c = O.rms_norm(np.full(512, -0.25), np.full(512, 3.0), 0.0)
+    assert np.allclose(c, -3.0, rtol=1e-15)
+
+
+def test_cache_rows_positions_and_rotary_key_properties():
+    rng = np.random.default_rng(4)
+    B, T = 2, 3
+    kv_a = rng.standard_normal((B, T, 576))
+    w = rng.standard_normal(512)
+    pos, lat, rot = O.cache_rows(kv_a, w, 1e-6, [5, 10], U_INV_FREQ)
+    assert np.array_equal(pos, [[2, 3, 4], [7, 8, 9]])
+    assert np.allclose(lat, O.rms_norm(kv_a[..., :512], w, 1e-6))
+    # a rotation: norms of the rotary key are kept
+    assert np.allclose(np.linalg.norm(rot, axis=-1), np.linalg.norm(kv_a[..., 512:], axis=-1), rtol=1e-13)
+    # a query and a key rotated at positions p and t score by p - t alone
+    q = rng.standard_normal(64)
+    k = kv_a[0, 0, 512:]
+    def score(p, t):
+        qr = O.rope_for_positions(q[None, None, :], [p + 1], U_INV_FREQ)[0, 0]
+        kr = O.cache_rows(np.concatenate([np.ones(512), k])[None, None, :], w, 1e-6, [t + 1], U_INV_FREQ)[2][0, 0]
+        return qr @ kr
+    assert abs(score(4, 4) - q @ k) < 1e-12
+    assert abs(score(9000, 8990) - score(10, 0)) < 1e-9
+    assert abs(score(9000, 8990) - score(10, 1)) > 1e-6
+
+
+def test_same_position_pin_catches_a_key_rotated_in_the_other_layout():
+    rng = np.random.default_rng(6)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    cis = O.freqs_cis(np.array([99]), U_INV_FREQ)[0]
+    qr = O.rope_for_positions(q[None, None, :], [100], U_INV_FREQ)[0, 0]
+    kr_good = O.cache_rows(np.concatenate([np.ones(512), k])[None, None, :], np.ones(512), 0.0, [100],
+                           U_INV_FREQ)[2][0, 0]
+    kr_bad = O.rope_half_split(k, cis)
+    assert abs(qr @ kr_good - q @ k) < 1e-12
+    assert abs(qr @ kr_bad - q @ k) > 1e-3

@@ -352,3 +352,94 @@ def test_decode_with_fp8_wkv_b_matches_oracle():
     x = U.oracle_inputs(t)
     x["wkv_b"] = O.dequant_to_bf16(codes.numpy(), scale.numpy(), 128)
     U.assert_attn_close(out.cpu().numpy(), U.oracle_out(x, list(range(B))), "decode with fp8 wkv_b")
+
+
+# ----------------------------------------------------------------- captured step
+def test_captured_step_replays_the_eager_step_exactly():
+    B, K = 5, 512
+    t = synth.make_inputs(synth.small_workload(B, [900, 512, 1000, 64, 777], k=K, K=K, S_cap=1024), seed=41)
+    d = _dev(t)
+    args = (d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    step = mla.DecodeStep(B, K)
+    eager = step(*args).clone()
+    g = mla.CapturedStep(step, *args)
+    assert g.kernels_per_replay == 3
+    d["q_nope"].mul_(-1)                      # new inputs in the captured buffers
+    out = g().clone()
+    torch.cuda.synchronize()
+    step.check_status()
+    x = U.oracle_inputs(t)
+    x["q_nope"] = -x["q_nope"]
+    U.assert_attn_close(out.cpu().numpy(), U.oracle_out(x, list(range(B))), "captured step, new inputs")
+    d["q_nope"].mul_(-1)
+    assert torch.equal(g().clone(), eager)
+
+
+# ----------------------------------------------------------------- cache append
+def _append_case(B, T, S_cap, end, seed):
+    g = torch.Generator().manual_seed(seed)
+    kv_a = (torch.randn(B, T, 576, generator=g) * 2.5).to(torch.bfloat16)
+    w = (1.0 + 0.1 * torch.randn(512, generator=g)).to(torch.bfloat16).float()
+    kv = torch.full((B, S_cap, 512), 7.0, dtype=torch.bfloat16)
+    pe = torch.full((B, S_cap, 64), 7.0, dtype=torch.bfloat16)
+    return kv_a, w, kv, pe, torch.tensor(end, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("B,T,S_cap,end", [(1, 1, 16, [1]), (4, 1, 1024, [1, 2, 1000, 1024]),
+                                           (3, 4, 4096, [4, 4096, 1234]), (130, 2, 64, [2 + b % 62 for b in range(130)])])
+def test_cache_append_matches_oracle(B, T, S_cap, end):
+    kv_a, w, kv, pe, end_pos = _append_case(B, T, S_cap, end, seed=B * 13 + T)
+    cis = mla.rope_freqs_init()
+    dkv, dpe = kv.cuda(), pe.cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_cache_append(kv_a.cuda(), w.cuda(), cis, end_pos.cuda(), dkv, dpe, eps=1e-6, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    pos, lat, rot = O.cache_rows(synth.to_f64(kv_a), w.double().numpy(), 1e-6, end_pos.numpy(), U.INV_FREQ)
+    got_kv, got_pe = dkv.cpu(), dpe.cpu()
+    written = torch.zeros(B, S_cap, dtype=torch.bool)
+    for b in range(B):
+        for s in range(T):
+            p = int(pos[b, s])
+            written[b, p] = True
+            gl = got_kv[b, p].double().numpy()
+            # bf16 rounding of the fp32 result: half an ulp (2^-8 relative) plus fp32 error
+            assert np.all(np.abs(gl - lat[b, s]) <= 2.0 ** -8 * np.abs(lat[b, s]) + 1e-5), (b, s)
+            gr = got_pe[b, p].double().numpy()
+            pair = np.repeat(np.hypot(rot[b, s, 0::2], rot[b, s, 1::2]), 2)
+            assert np.all(np.abs(gr - rot[b, s]) <= 2.0 ** -8 * np.abs(rot[b, s]) + 1e-5 * pair), (b, s)
+    # nothing else was touched
+    assert torch.all(got_kv[~written] == 7.0) and torch.all(got_pe[~written] == 7.0)
+
+
+def test_cache_append_then_decode_reads_the_new_rows():
+    B, S_cap, K = 2, 512, 128
+    t = synth.make_inputs(synth.small_workload(B, [300, 511], k=K, K=K, S_cap=S_cap), seed=43)
+    kv_a, w, _, _, _ = _append_case(B, 1, S_cap, [1, 1], seed=44)
+    end_pos = t["end_pos"] + 1                    # one new token per sequence
+    t["topk_idx"][:, 0] = end_pos - 1             # the new token is selected
+    d = _dev(t)
+    cis = mla.rope_freqs_init()
+    mla.mla_cache_append(kv_a.cuda(), w.cuda(), cis, end_pos.cuda(), d["kv_cache"], d["pe_cache"])
+    step = mla.DecodeStep(B, K)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], end_pos.cuda())
+    torch.cuda.synchronize()
+    step.check_status()
+    x = U.oracle_inputs(t)
+    x["end_pos"] = end_pos.numpy().astype(np.int64)
+    # the oracle reads the appended rows the GPU wrote (bf16, checked above)
+    x["kv_cache"] = synth.to_f64(d["kv_cache"].cpu())
+    x["pe_cache"] = synth.to_f64(d["pe_cache"].cpu())
+    U.assert_attn_close(out.cpu().numpy(), U.oracle_out(x, list(range(B))), "decode after append")
+
+
+def test_cache_append_reports_and_skips_bad_positions():
+    kv_a, w, kv, pe, _ = _append_case(3, 2, 64, [2, 2, 2], seed=5)
+    dkv, dpe = kv.cuda(), pe.cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cis = mla.rope_freqs_init(mla.rope_params(max_seq_len=32))
+    end = torch.tensor([1, 65, 40], dtype=torch.int32, device="cuda")   # < T, > S_cap, beyond the table
+    mla.mla_cache_append(kv_a.cuda(), w.cuda(), cis, end, dkv, dpe, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == mla.MLA_DEV_BAD_END_POS | mla.MLA_DEV_BAD_POSITION
+    assert torch.all(dkv.cpu() == 7.0) and torch.all(dpe.cpu() == 7.0)
