@@ -147,8 +147,21 @@ int mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const float *cis,
                  const int32_t *end_pos, const mla_bf16 *wkv_b, int B, mla_bf16 *q_lat,
                  int32_t *dev_status, mla_stream_t stream);
 
-/* Bytes of device workspace mla_sparse_decode needs for B sequences whose
- * selection rows hold K entries.  0 when B or K is out of range. */
+/* mla_absorb_q_tokens -- mla_absorb_q for T query tokens per sequence
+ * (multi-token decode).  Row r = b*T + s is token s of sequence b; its
+ * rotary part is rotated at position end_pos[b] - T + s.
+ *   q_nope [n_seq][T][128][128], q_pe [n_seq][T][128][64] bf16,
+ *   end_pos [n_seq] int32 (cached tokens AFTER the T new ones),
+ *   q_lat [n_seq][T][128][576] bf16 (written).  T = 1 is mla_absorb_q.
+ * Errors: as mla_absorb_q, with MLA_ERR_SIZE for n_seq or T < 1 or
+ * n_seq*T > 4096. */
+int mla_absorb_q_tokens(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const float *cis, int max_seq_len,
+                        const int32_t *end_pos, const mla_bf16 *wkv_b, int n_seq, int T, mla_bf16 *q_lat,
+                        int32_t *dev_status, mla_stream_t stream);
+
+/* Bytes of device workspace mla_sparse_decode needs for B query rows (B
+ * sequences, or n_seq*T rows for mla_sparse_decode_tokens) whose selection
+ * rows hold K entries.  0 when B or K is out of range. */
 size_t mla_sparse_decode_workspace_size(int B, int K);
 
 /* mla_sparse_decode -- scores of every head against the selected rows of the
@@ -176,6 +189,26 @@ int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla
                       int S_cap, const int32_t *topk_idx, int K, const int32_t *end_pos, int B,
                       float softmax_scale, const mla_bf16 *wkv_b, float *out, void *workspace,
                       size_t ws_bytes, int32_t *dev_status, mla_stream_t stream);
+
+/* mla_sparse_decode_tokens -- mla_sparse_decode for T query tokens per
+ * sequence (multi-token decode; the "Attention weights" page notes that the
+ * causal mask is merged into the selection).  Row r = b*T + s is token s of
+ * sequence b, at position pos = end_pos[b] - T + s; it attends to the
+ * positions of its own selection row topk_idx[r] that are <= pos (the
+ * selection merged with the causal mask; entries > pos count as padding).
+ *   q_lat    [n_seq][T][128][576] bf16 (mla_absorb_q_tokens)
+ *   kv_cache [n_seq][S_cap][512], pe_cache [n_seq][S_cap][64] bf16 (the T new
+ *            rows already appended, e.g. by mla_cache_append)
+ *   topk_idx [n_seq][T][K] int32, end_pos [n_seq] int32 (T <= end_pos <= S_cap,
+ *            else MLA_DEV_BAD_END_POS and zeros for that sequence)
+ *   out      [n_seq][T][128][128] (wkv_b given) or [n_seq][T][128][512] fp32
+ *   workspace at least mla_sparse_decode_workspace_size(n_seq*T, K) bytes.
+ * T = 1 is mla_sparse_decode.  Errors: as mla_sparse_decode, with
+ * MLA_ERR_SIZE for n_seq or T < 1 or n_seq*T > 4096. */
+int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla_bf16 *pe_cache, int S_cap,
+                             const int32_t *topk_idx, int K, const int32_t *end_pos, int n_seq, int T,
+                             float softmax_scale, const mla_bf16 *wkv_b, float *out, void *workspace,
+                             size_t ws_bytes, int32_t *dev_status, mla_stream_t stream);
 
 /* mla_out_up -- value up-projection alone ("Attention weights" page, excerpt
  * mla-decode, last einsum): out[b,h,d] = sum_c o_lat[b,h,c] * W_UV[h][d][c],

@@ -304,6 +304,63 @@ def decode_step(q_nope, q_pe, kv_cache, pe_cache, wkv_b, topk_idx, end_pos, inv_
 
 
 # --------------------------------------------------------------------------
+# Multi-token decode: T query tokens per sequence.  The "Attention weights"
+# page notes that the causal mask is added to the selection before the
+# softmax; the plain reading for T tokens is that token s of sequence b sits at
+# position end_pos[b] - T + s, has its own selection row, and sees a key t only
+# if t is selected AND t <= its position.
+# --------------------------------------------------------------------------
+def token_positions(end_pos: int, T: int) -> np.ndarray:
+    return int(end_pos) - T + np.arange(T)
+
+
+def attend_tokens(q_abs: np.ndarray, q_pe_rot: np.ndarray, kv: np.ndarray, pe: np.ndarray,
+                  topk_rows: np.ndarray, end_pos: int, scale: float) -> np.ndarray:
+    """T tokens of one sequence: q_abs [T,H,512], q_pe_rot [T,H,64],
+    topk_rows [T,K].  Scores over all end_pos keys plus the index mask (0 on
+    each token's selection, -inf elsewhere) plus the causal mask (-inf on keys
+    after the token's position), softmax over keys, PV.  Returns [T,H,512]."""
+    T = q_abs.shape[0]
+    kv, pe = kv[:end_pos], pe[:end_pos]
+    scores = (np.einsum("shc,tc->sht", q_abs, kv) + np.einsum("shr,tr->sht", q_pe_rot, pe)) * scale
+    index_mask = np.full((T, end_pos), -np.inf)
+    for s in range(T):
+        idx = np.asarray(topk_rows[s], dtype=np.int64)
+        idx = idx[(idx >= 0) & (idx < end_pos)]
+        index_mask[s, idx] = 0.0
+    pos = token_positions(end_pos, T)
+    causal = np.where(np.arange(end_pos)[None, :] <= pos[:, None], 0.0, -np.inf)
+    mask = index_mask + causal                         # [T, end_pos]
+    out = np.zeros((T, q_abs.shape[1], kv.shape[1]))
+    for s in range(T):
+        sel = np.isfinite(mask[s])
+        if not sel.any():
+            continue                                   # nothing visible: zeros
+        z = scores[s][:, sel]
+        p = np.exp(z - z.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        out[s] = p @ kv[sel]
+    return out
+
+
+def decode_tokens(q_nope, q_pe, kv_cache, pe_cache, wkv_b, topk_idx, end_pos, inv_freq, scale, batches=None):
+    """Full step for T tokens per sequence: q_nope [n,T,H,128], q_pe [n,T,H,64],
+    topk_idx [n,T,K], end_pos [n] (cached tokens including the T new ones).
+    Returns out [len(batches),T,H,128]."""
+    bs = list(range(q_nope.shape[0])) if batches is None else list(batches)
+    T = q_nope.shape[1]
+    res = []
+    for b in bs:
+        pos = token_positions(end_pos[b], T)
+        q_abs = absorb(q_nope[b], wkv_b)                                   # [T,H,512]
+        cis = freqs_cis(pos, inv_freq)[:, None, :]
+        q_rot = rope_interleaved(q_pe[b], cis)                             # [T,H,64]
+        o = attend_tokens(q_abs, q_rot, kv_cache[b], pe_cache[b], topk_idx[b], int(end_pos[b]), scale)
+        res.append(out_up(o, wkv_b))
+    return np.stack(res)
+
+
+# --------------------------------------------------------------------------
 # Cache append ("Query heads" page, excerpt mla-init and its prose: wkv_a
 # emits the 512 latent features and the 64-wide rotary key, kv_norm is an
 # RMSNorm of the latent; "Attention weights" page, excerpt mla-decode: the

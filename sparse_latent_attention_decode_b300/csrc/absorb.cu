@@ -34,11 +34,12 @@ struct Bars {
     uint32_t tmem_base;
 };
 
-// Interleaved rotation of pairs [8t, 8t+8) of q_pe[b, h] for every sequence,
-// four items per thread at a time so that the loads overlap.
+// Interleaved rotation of pairs [8t, 8t+8) of q_pe[b, h] for every query row,
+// four items per thread at a time so that the loads overlap.  Row b is token
+// b % T of sequence b / T, at position end_pos[b / T] - T + b % T.
 __device__ __forceinline__ void rope_part(const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis,
-                                          int max_seq_len, const int32_t *__restrict__ end_pos, int B, int h,
-                                          int t, uint16_t *__restrict__ q_lat, int32_t *status, int tid) {
+                                          int max_seq_len, const int32_t *__restrict__ end_pos, int B, int T,
+                                          int h, int t, uint16_t *__restrict__ q_lat, int32_t *status, int tid) {
     constexpr int BATCH = 4;
     const int total = B * PAIRS_PER_TILE;
     for (int k0 = tid; k0 < total; k0 += 128 * BATCH) {
@@ -46,7 +47,8 @@ __device__ __forceinline__ void rope_part(const uint16_t *__restrict__ q_pe, con
 #pragma unroll
         for (int u = 0; u < BATCH; ++u) {
             const int k = k0 + 128 * u;
-            pos[u] = k < total ? end_pos[k / PAIRS_PER_TILE] - 1 : -1;
+            const int row = k / PAIRS_PER_TILE, seq = row / T;
+            pos[u] = k < total ? end_pos[seq] - T + (row - seq * T) : -1;
         }
         uint32_t w[BATCH];
         float2 cs[BATCH];
@@ -75,7 +77,7 @@ __device__ __forceinline__ void rope_part(const uint16_t *__restrict__ q_pe, con
 __global__ void __launch_bounds__(128)
     absorb_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
                   const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis, int max_seq_len,
-                  const int32_t *__restrict__ end_pos, int B, uint16_t *__restrict__ q_lat, int32_t *status) {
+                  const int32_t *__restrict__ end_pos, int B, int T, uint16_t *__restrict__ q_lat, int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(128)
             tma_load_3d(smem_u32(sB), &qmap, 0, h, n0, &bars.b_full);
             tma_load_3d(smem_u32(sB + B_BOX), &qmap, 64, h, n0, &bars.b_full);
         }
-        if (pass == 0) rope_part(q_pe, cis, max_seq_len, end_pos, B, h, t, q_lat, status, tid);
+        if (pass == 0) rope_part(q_pe, cis, max_seq_len, end_pos, B, T, h, t, q_lat, status, tid);
         if (tid == 0) {
             bool good = wait_until(&bars.b_full, pass & 1, deadline);
             if (pass == 0) good = good && wait_until(&bars.a_full, 0, deadline);
@@ -170,13 +172,14 @@ __global__ void __launch_bounds__(128)
 
 using namespace mla;
 
-extern "C" int mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const float *cis, int max_seq_len,
-                            const int32_t *end_pos, const mla_bf16 *wkv_b, int B, mla_bf16 *q_lat,
-                            int32_t *dev_status, mla_stream_t stream) {
+extern "C" int mla_absorb_q_tokens(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const float *cis,
+                                   int max_seq_len, const int32_t *end_pos, const mla_bf16 *wkv_b, int n_seq, int T,
+                                   mla_bf16 *q_lat, int32_t *dev_status, mla_stream_t stream) {
     if (!q_nope || !q_pe || !cis || !end_pos || !wkv_b || !q_lat) return MLA_ERR_NULL;
     if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(cis) || !aligned16(wkv_b) || !aligned16(q_lat))
         return MLA_ERR_ALIGN;
-    if (B < 1 || B > 4096 || max_seq_len < 1) return MLA_ERR_SIZE;
+    if (n_seq < 1 || T < 1 || (long long)n_seq * T > 4096 || max_seq_len < 1) return MLA_ERR_SIZE;
+    const int B = n_seq * T;   // query rows
     CUtensorMap wmap, qmap;
     {
         const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
@@ -201,7 +204,13 @@ extern "C" int mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const 
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     absorb::absorb_kernel<<<dim3(4, H), 128, absorb::SMEM_BYTES, s>>>(
-        wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, q_lat, dev_status);
+        wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, T, q_lat, dev_status);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+extern "C" int mla_absorb_q(const mla_bf16 *q_nope, const mla_bf16 *q_pe, const float *cis, int max_seq_len,
+                            const int32_t *end_pos, const mla_bf16 *wkv_b, int B, mla_bf16 *q_lat,
+                            int32_t *dev_status, mla_stream_t stream) {
+    return mla_absorb_q_tokens(q_nope, q_pe, cis, max_seq_len, end_pos, wkv_b, B, 1, q_lat, dev_status, stream);
 }

@@ -95,7 +95,8 @@ struct Params {
     const uint16_t *pe;
     const int32_t *topk;
     const int32_t *end_pos;
-    int S_cap, K, B;
+    int S_cap, K, B;    // B: query rows, T per sequence (row b is token b % T of sequence b / T)
+    int T;
     float scale_log2;   // softmax_scale * log2(e)
     int n_split, split_len;   // split_len <= IDX_CAP
     float *o_out;       // n_split == 1: normalised o, fp32 [B][128][512] (or NULL)
@@ -141,9 +142,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     // before it has completed.
     grid_dep_wait();
     const int unit = blockIdx.x >> 1;
-    const int b = unit / p.n_split, split = unit % p.n_split;
-    const int e = p.end_pos[b];
-    const bool seq_ok = e >= 1 && e <= p.S_cap;
+    const int b = unit / p.n_split, split = unit % p.n_split;   // query row
+    const int cb = b / p.T;                                     // its sequence in the caches
+    const int e_seq = p.end_pos[cb];
+    const bool seq_ok = e_seq >= p.T && e_seq <= p.S_cap;
+    // keys [0, e) are visible to the row: the selection merged with the causal mask
+    const int e = e_seq - p.T + (b - cb * p.T) + 1;
     const int t0 = split * p.split_len;
     const int t1 = min(p.K, t0 + p.split_len);
     const int nblk = (seq_ok && t1 > t0) ? (t1 - t0 + NK - 1) / NK : 0;
@@ -213,8 +217,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 pe_mask |= 1u << q;
             }
         }
-        const uint16_t *kvb = p.kv + (size_t)b * p.S_cap * C;
-        const uint16_t *peb = p.pe + (size_t)b * p.S_cap * DR;
+        const uint16_t *kvb = p.kv + (size_t)cb * p.S_cap * C;
+        const uint16_t *peb = p.pe + (size_t)cb * p.S_cap * DR;
         for (int j = 0; j < nblk; ++j) {
             const int s = j % NS;
             if (j >= NS && !warp_wait(&bars.empty[s], ((j / NS) - 1) & 1, deadline)) {
@@ -579,7 +583,7 @@ size_t attn_workspace(int B, int K, int *n_split_out, int *split_len_out) {
 }
 
 int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, int S_cap, const int32_t *topk, int K,
-                const int32_t *end_pos, int B, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
+                const int32_t *end_pos, int B, int T, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
                 int32_t *status, cudaStream_t s, int *launches) {
     int n_split = 1, split_len = K;
     attn_workspace(B, K, &n_split, &split_len);
@@ -592,6 +596,7 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
     p.S_cap = S_cap;
     p.K = K;
     p.B = B;
+    p.T = T;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.n_split = n_split;
     p.split_len = split_len;

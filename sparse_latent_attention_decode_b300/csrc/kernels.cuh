@@ -13,13 +13,15 @@ namespace mla {
 int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
                   int32_t *status, cudaStream_t s, bool pdl);
 
-// Sparse attention (tensor-core kernel + split combine).  Writes the
-// normalised latent output o [B][128][512] as fp32 to o_out or as bf16 to
-// o_b16 (exactly one non-NULL).  ws must hold attn_workspace(B, K) bytes
-// (256-byte aligned).
+// Sparse attention (tensor-core kernel + split combine) over B query rows,
+// T per sequence: row b is token b % T of cache sequence b / T, at position
+// end_pos[b / T] - T + b % T, and sees the selected keys up to that position.
+// Writes the normalised latent output o [B][128][512] as fp32 to o_out or as
+// bf16 to o_b16 (exactly one non-NULL).  ws must hold attn_workspace(B, K)
+// bytes (256-byte aligned).
 size_t attn_workspace(int B, int K, int *n_split = nullptr, int *split_len = nullptr);
 int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, int S_cap, const int32_t *topk, int K,
-                const int32_t *end_pos, int B, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
+                const int32_t *end_pos, int B, int T, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
                 int32_t *status, cudaStream_t s, int *launches);
 
 // Launch `kern` on stream s.  With pdl set, the launch allows programmatic

@@ -57,6 +57,8 @@ def _load():
         "mla_sparse_decode_static_ws": (I, [P, P, P, I, P, I, P, I, F, P, P, P, P]),
         "mla_weight_dequant_fp8": (I, [P, P, I, I, I, P, P]),
         "mla_cache_append": (I, [P, P, F, P, I, P, I, I, P, P, I, P, P]),
+        "mla_absorb_q_tokens": (I, [P, P, P, I, P, P, I, I, P, P, P]),
+        "mla_sparse_decode_tokens": (I, [P, P, P, I, P, I, P, I, I, F, P, P, P, Z, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -70,7 +72,7 @@ _lib = _load()
 EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply", "mla_rope_apply_layout",
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
             "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws", "mla_weight_dequant_fp8",
-            "mla_cache_append")
+            "mla_cache_append", "mla_absorb_q_tokens", "mla_sparse_decode_tokens")
 STATIC_WS_BYTES = 32 << 20
 
 
@@ -207,6 +209,51 @@ def mla_cache_append(kv_a, kv_norm_w, cis, end_pos, kv_cache, pe_cache, eps: flo
     _check(_lib.mla_cache_append(_ptr(kv_a), _ptr(kv_norm_w), float(eps), _ptr(cis), cis.shape[0], _ptr(end_pos),
                                  B, T, _ptr(kv_cache), _ptr(pe_cache), S_cap, _ptr(dev_status),
                                  _stream(kv_a.device)), "mla_cache_append")
+
+
+def mla_absorb_q_tokens(q_nope, q_pe, cis, end_pos, wkv_b, out=None, dev_status=None) -> torch.Tensor:
+    """mla_absorb_q for T tokens per sequence: q_nope [n, T, 128, 128],
+    q_pe [n, T, 128, 64]; token s of sequence b is rotated at end_pos[b] - T + s."""
+    n, T = q_nope.shape[0], q_nope.shape[1]
+    _need(q_nope, "q_nope", torch.bfloat16, (n, T, N_HEADS, D_NOPE))
+    _need(q_pe, "q_pe", torch.bfloat16, (n, T, N_HEADS, D_ROPE))
+    _need(cis, "cis", torch.float32)
+    _need(end_pos, "end_pos", torch.int32, (n,))
+    _need(wkv_b, "wkv_b", torch.bfloat16, (N_HEADS * (D_NOPE + D_V), KV_LORA))
+    if out is None:
+        out = torch.empty(n, T, N_HEADS, Q_LAT, dtype=torch.bfloat16, device=q_nope.device)
+    _need(out, "q_lat", torch.bfloat16, (n, T, N_HEADS, Q_LAT))
+    _check(_lib.mla_absorb_q_tokens(_ptr(q_nope), _ptr(q_pe), _ptr(cis), cis.shape[0], _ptr(end_pos), _ptr(wkv_b),
+                                    n, T, _ptr(out), _ptr(dev_status), _stream(q_nope.device)),
+           "mla_absorb_q_tokens")
+    return out
+
+
+def mla_sparse_decode_tokens(q_lat, kv_cache, pe_cache, topk_idx, end_pos, softmax_scale, wkv_b=None, out=None,
+                             workspace=None, dev_status=None) -> torch.Tensor:
+    """mla_sparse_decode for T tokens per sequence: q_lat [n, T, 128, 576],
+    topk_idx [n, T, K]; token s of sequence b sees its selected positions up to
+    end_pos[b] - T + s.  Returns [n, T, 128, 128] (or [n, T, 128, 512])."""
+    n, T, K = topk_idx.shape
+    S_cap = kv_cache.shape[1]
+    _need(q_lat, "q_lat", torch.bfloat16, (n, T, N_HEADS, Q_LAT))
+    _need(kv_cache, "kv_cache", torch.bfloat16, (n, S_cap, KV_LORA))
+    _need(pe_cache, "pe_cache", torch.bfloat16, (n, S_cap, D_ROPE))
+    _need(topk_idx, "topk_idx", torch.int32, (n, T, K))
+    _need(end_pos, "end_pos", torch.int32, (n,))
+    if wkv_b is not None:
+        _need(wkv_b, "wkv_b", torch.bfloat16, (N_HEADS * (D_NOPE + D_V), KV_LORA))
+    width = D_V if wkv_b is not None else KV_LORA
+    if out is None:
+        out = torch.empty(n, T, N_HEADS, width, dtype=torch.float32, device=q_lat.device)
+    _need(out, "out", torch.float32, (n, T, N_HEADS, width))
+    if workspace is None:
+        workspace = torch.empty(workspace_size(n * T, K), dtype=torch.uint8, device=q_lat.device)
+    _check(_lib.mla_sparse_decode_tokens(_ptr(q_lat), _ptr(kv_cache), _ptr(pe_cache), S_cap, _ptr(topk_idx), K,
+                                         _ptr(end_pos), n, T, float(softmax_scale), _ptr(wkv_b), _ptr(out),
+                                         _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                         _stream(q_lat.device)), "mla_sparse_decode_tokens")
+    return out
 
 
 def workspace_size(B: int, K: int) -> int:

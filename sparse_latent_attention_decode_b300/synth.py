@@ -149,6 +149,27 @@ def make_inputs(wl: Workload, seed: int = 0, fill_tail: bool = False, threads: i
                 topk_idx=topk, end_pos=end_pos)
 
 
+def make_token_inputs(wl: Workload, T: int, seed: int = 0, threads: int = 8) -> dict:
+    """make_inputs for T query tokens per sequence (multi-token decode):
+    q_nope [B,T,128,128], q_pe [B,T,128,64] and topk_idx [B,T,K]; each token
+    draws its own selection over all end_pos[b] cached positions (positions
+    after the token's own are left in, as an indexer run before the causal
+    mask would), the caches, wkv_b and end_pos are those of make_inputs."""
+    t = make_inputs(wl, seed, threads=threads)
+    B, K = wl.B, wl.row_stride()
+    q_nope = torch.empty(B, T, N_HEADS, D_NOPE, dtype=torch.bfloat16)
+    q_pe = torch.empty(B, T, N_HEADS, D_ROPE, dtype=torch.bfloat16)
+    topk = torch.full((B, T, K), -1, dtype=torch.int32)
+    for b in range(B):
+        q_nope[b] = _randn_bf16((T, N_HEADS, D_NOPE), _gen(seed, "tok/q_nope", b))
+        q_pe[b] = _randn_bf16((T, N_HEADS, D_ROPE), _gen(seed, "tok/q_pe", b))
+        for s in range(T):
+            sel = draw_topk(seed + 7919 * (s + 1), b, wl.end_pos[b], wl.k_of(b), wl.selection)
+            topk[b, s, : sel.numel()] = sel
+    t.update(q_nope=q_nope, q_pe=q_pe, topk_idx=topk)
+    return t
+
+
 def make_fp8_weight(seed: int, rows: int = N_HEADS * (D_NOPE + D_V), cols: int = KV_LORA, block: int = 128,
                     name: str = "wkv_b_fp8"):
     """A block-scaled fp8 weight: e4m3 codes [rows, cols] (uint8) and fp32

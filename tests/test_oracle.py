@@ -477,3 +477,58 @@ def test_same_position_pin_catches_a_key_rotated_in_the_other_layout():
     kr_bad = O.rope_half_split(k, cis)
     assert abs(qr @ kr_good - q @ k) < 1e-12
     assert abs(qr @ kr_bad - q @ k) > 1e-3
+
+
+# ----------------------------------------------------------------- multi-token decode
+def _tok_case(T, seed=9, end=(300, 41)):
+    wl = synth.small_workload(len(end), list(end), k=40, K=40, S_cap=320)
+    t = synth.make_token_inputs(wl, T, seed=seed)
+    return {k: synth.to_f64(v) for k, v in t.items()}
+
+
+def test_one_token_decode_is_the_single_token_step():
+    x = _tok_case(1)
+    got = O.decode_tokens(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"], x["topk_idx"],
+                          x["end_pos"], U_INV_FREQ, O.softmax_scale())
+    ref = O.decode_step(x["q_nope"][:, 0], x["q_pe"][:, 0], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                        x["topk_idx"][:, 0], x["end_pos"], U_INV_FREQ, O.softmax_scale())
+    assert np.allclose(got[:, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_each_token_is_a_single_token_step_at_its_own_position():
+    T = 4
+    x = _tok_case(T)
+    got = O.decode_tokens(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"], x["topk_idx"],
+                          x["end_pos"], U_INV_FREQ, O.softmax_scale())
+    for s in range(T):
+        ep = x["end_pos"] - T + s + 1
+        ref = O.decode_step(x["q_nope"][:, s], x["q_pe"][:, s], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                            x["topk_idx"][:, s], ep, U_INV_FREQ, O.softmax_scale())
+        assert np.allclose(got[:, s], ref, rtol=1e-12, atol=1e-12), s
+
+
+def test_multi_token_outputs_are_causal():
+    T = 3
+    x = _tok_case(T, end=(60,))
+    x["topk_idx"][0, :, :3] = [57, 58, 59]               # every token selects the three new positions
+    args = lambda: (x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"], x["topk_idx"],
+                    x["end_pos"], U_INV_FREQ, O.softmax_scale())
+    before = O.decode_tokens(*args())
+    x["kv_cache"][0, 59] *= -3.0                          # the last token's own row
+    x["pe_cache"][0, 59] += 1.0
+    after = O.decode_tokens(*args())
+    assert np.array_equal(before[0, :2], after[0, :2])    # tokens at 57 and 58 cannot see position 59
+    assert not np.allclose(before[0, 2], after[0, 2])
+
+
+def test_position_pin_catches_tokens_placed_at_the_last_position(monkeypatch):
+    # plant: every token placed at end_pos - 1 (no causal mask, one rotation)
+    T = 3
+    x = _tok_case(T, end=(60,))
+    x["topk_idx"][0, :, :3] = [57, 58, 59]
+    monkeypatch.setattr(O, "token_positions", lambda end_pos, T: int(end_pos) - 1 + 0 * np.arange(T))
+    got = O.decode_tokens(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"], x["topk_idx"],
+                          x["end_pos"], U_INV_FREQ, O.softmax_scale())
+    ref = O.decode_step(x["q_nope"][:, 0], x["q_pe"][:, 0], x["kv_cache"], x["pe_cache"], x["wkv_b"],
+                        x["topk_idx"][:, 0], x["end_pos"] - T + 1, U_INV_FREQ, O.softmax_scale())
+    assert not np.allclose(got[:, 0], ref, rtol=1e-12, atol=1e-12)

@@ -443,3 +443,61 @@ def test_cache_append_reports_and_skips_bad_positions():
     torch.cuda.synchronize()
     assert int(st.item()) == mla.MLA_DEV_BAD_END_POS | mla.MLA_DEV_BAD_POSITION
     assert torch.all(dkv.cpu() == 7.0) and torch.all(dpe.cpu() == 7.0)
+
+
+# ----------------------------------------------------------------- multi-token decode
+TOKENS = [
+    # (end_pos per sequence, T, k, K)
+    ([300, 41], 2, 40, 40),
+    ([1000, 64, 777], 4, 256, 256),
+    ([2048, 1500], 3, 1100, 1100),       # several splits per query row
+    ([5, 9, 600, 4096] * 5, 2, 300, 320),  # 40 query rows, ragged K tail
+]
+
+
+@pytest.mark.parametrize("case", TOKENS, ids=[f"n{len(c[0])}_T{c[1]}_K{c[3]}" for c in TOKENS])
+def test_multi_token_decode_matches_oracle(case):
+    ends, T, k, K = case
+    S = max(ends)
+    wl = synth.small_workload(len(ends), ends, k=k, K=K, S_cap=S)
+    t = synth.make_token_inputs(wl, T, seed=47)
+    d = _dev(t)
+    cis = mla.rope_freqs_init()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_lat = mla.mla_absorb_q_tokens(d["q_nope"], d["q_pe"], cis, d["end_pos"], d["wkv_b"], dev_status=st)
+    out = mla.mla_sparse_decode_tokens(q_lat, d["kv_cache"], d["pe_cache"], d["topk_idx"], d["end_pos"], U.SCALE,
+                                       wkv_b=d["wkv_b"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    x = U.oracle_inputs(t)
+    ora = O.decode_tokens(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], x["wkv_b"], x["topk_idx"],
+                          x["end_pos"], U.INV_FREQ, U.SCALE)
+    U.assert_attn_close(out.cpu().numpy().reshape(-1, 128, 128), ora.reshape(-1, 128, 128), "multi-token")
+
+
+def test_multi_token_one_token_equals_the_single_token_entry():
+    B, K = 6, 512
+    t = synth.make_inputs(synth.small_workload(B, [900, 512, 1000, 64, 777, 1], k=K, K=K, S_cap=1024), seed=53)
+    d = _dev(t)
+    cis = mla.rope_freqs_init()
+    q1 = mla.mla_absorb_q(d["q_nope"], d["q_pe"], cis, d["end_pos"], d["wkv_b"])
+    qt = mla.mla_absorb_q_tokens(d["q_nope"][:, None], d["q_pe"][:, None], cis, d["end_pos"], d["wkv_b"])
+    assert torch.equal(q1, qt[:, 0])
+    o1 = mla.mla_sparse_decode(q1, d["kv_cache"], d["pe_cache"], d["topk_idx"], d["end_pos"], U.SCALE, wkv_b=d["wkv_b"])
+    ot = mla.mla_sparse_decode_tokens(qt, d["kv_cache"], d["pe_cache"], d["topk_idx"][:, None], d["end_pos"], U.SCALE,
+                                      wkv_b=d["wkv_b"])
+    assert torch.equal(o1, ot[:, 0])
+
+
+def test_multi_token_bad_end_pos_is_reported():
+    wl = synth.small_workload(2, [3, 100], k=3, K=3, S_cap=100)
+    t = synth.make_token_inputs(wl, 4, seed=2)
+    d = _dev(t)
+    cis = mla.rope_freqs_init()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_lat = mla.mla_absorb_q_tokens(d["q_nope"], d["q_pe"], cis, d["end_pos"], d["wkv_b"], dev_status=st)
+    out = mla.mla_sparse_decode_tokens(q_lat, d["kv_cache"], d["pe_cache"], d["topk_idx"], d["end_pos"], U.SCALE,
+                                       wkv_b=d["wkv_b"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & mla.MLA_DEV_BAD_END_POS       # end_pos 3 < T = 4
+    assert torch.all(out[0] == 0) and torch.any(out[1] != 0)
