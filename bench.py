@@ -271,7 +271,68 @@ def measure_next_rows(mla, synth, dev, flush, seed: int, n: int = 50) -> dict:
     out["weight_dequant_fp8"] = {"workload": "wkv_b 32768 x 512 e4m3, fp32 scale per 128 x 128 tile",
                                  "kernel_ms": ms, "alg_bytes_per_launch": nbytes,
                                  "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
+    del codes, scale, w
+    # cache append of one new token for 64 sequences (RMSNorm + rotary key)
+    S_app = 4096
+    kv_a = torch.randn(B, 1, 576, generator=g).to(torch.bfloat16).to(dev)
+    norm_w = torch.ones(512, dtype=torch.float32, device=dev)
+    kvc = torch.zeros(B, S_app, 512, dtype=torch.bfloat16, device=dev)
+    pec = torch.zeros(B, S_app, 64, dtype=torch.bfloat16, device=dev)
+    end_a = torch.randint(1, S_app + 1, (B,), generator=g, dtype=torch.int32).to(dev)
+    ms = time_single_kernel(lambda: mla.mla_cache_append(kv_a, norm_w, cis, end_a, kvc, pec), n, flush)
+    nbytes = B * (576 * 2 + 512 * 2 + 64 * 2 + 32 * 8 + 4) + 512 * 4
+    out["cache_append"] = {"workload": f"B={B}, 1 token each, S_cap {S_app}", "kernel_ms": ms,
+                           "alg_bytes_per_launch": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
+    del kvc, pec
+    # the projections around the attention; the model width 7168 is the
+    # DeepSeek-V3 value (the pages leave dim out)
+    for name, (M, N, K) in (("linear_wkv_a", (B, 576, 7168)), ("linear_wo", (B, 7168, 128 * 128))):
+        x, w = synth.make_linear_inputs(seed, M, N, K, name=name)
+        x, w = x.to(dev), w.to(dev)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(mla.linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+        ms = time_single_kernel(lambda: mla.mla_linear_bf16(x, w, out_dtype=torch.bfloat16, out=y, workspace=ws),
+                                n, flush)
+        nbytes = (N * K + M * K + M * N) * 2
+        out[name] = {"workload": f"M={M} tokens, N={N}, K={K}, bf16 in and out (weight and split-K reduction "
+                                 f"in one timed call)", "kernel_ms": ms, "alg_bytes_per_launch": nbytes,
+                     "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
+        del x, w, y, ws
     return out
+
+
+def measure_multi_token(mla, step, d, B, K, rows, flush, n: int = 50) -> dict:
+    """Multi-token decode over the bench caches: B/2 sequences x 2 query tokens
+    (the step's own q_lat and selections regrouped), the attention kernel
+    timed alone by the library's events around it."""
+    n_seq, T = B // 2, 2
+    q = step.q_lat.view(n_seq, T, 128, 576)
+    top = d["topk_idx"].view(n_seq, T, K)
+    end = d["end_pos"][:n_seq].contiguous()
+    kv, pe = d["kv_cache"][:n_seq], d["pe_cache"][:n_seq]
+    out = torch.empty(n_seq, T, 128, 128, dtype=torch.float32, device=q.device)
+    ws = torch.empty(mla.workspace_size(n_seq * T, K), dtype=torch.uint8, device=q.device)
+    call = lambda: mla.mla_sparse_decode_tokens(q, kv, pe, top, end, step.scale, wkv_b=d["wkv_b"], out=out,
+                                                workspace=ws)
+    for i in range(3):
+        call()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    for e in ev:
+        e.record()
+    torch.cuda.synchronize()
+    with mla.ProfileHook() as hook:
+        for i in range(n):
+            flush.fill_((i + 13) & 0xFF)
+            hook.set_events(ev[2 * i], ev[2 * i + 1])
+            call()
+    torch.cuda.synchronize()
+    ms = statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n))
+    # selected rows a token can see: its selection minus positions after it
+    pos = end[:, None].long() - T + torch.arange(T, device=q.device)[None, :]
+    vis = int(((top >= 0) & (top.long() <= pos[:, :, None])).sum().item())
+    nbytes = vis * ROW_BYTES
+    return {"workload": f"{n_seq} sequences x {T} tokens, end_pos {int(end[0])}, top-{K} per token, causal",
+            "kernel_ms": ms, "alg_bytes_per_launch": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
 
 
 def run_ours(args):
@@ -364,6 +425,8 @@ def run_ours(args):
                             world, dev)
 
     next_rows = measure_next_rows(mla, synth, dev, flush, args.seed)
+    if B % 2 == 0:
+        next_rows["multi_token_decode"] = measure_multi_token(mla, step, d, B, K, rows, flush)
 
     if rank != 0:
         return None

@@ -201,13 +201,17 @@ int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla
  *            rows already appended, e.g. by mla_cache_append)
  *   topk_idx [n_seq][T][K] int32, end_pos [n_seq] int32 (T <= end_pos <= S_cap,
  *            else MLA_DEV_BAD_END_POS and zeros for that sequence)
- *   out      [n_seq][T][128][128] (wkv_b given) or [n_seq][T][128][512] fp32
+ *   out      [n_seq][T][128][128] (wkv_b given) or [n_seq][T][128][512]:
+ *            fp32 when out_bf16 = 0, bf16 (rounded once from the fp32
+ *            result) when out_bf16 = 1 -- the form mla_linear_bf16 takes as
+ *            the input of the output projection wo.
  *   workspace at least mla_sparse_decode_workspace_size(n_seq*T, K) bytes.
- * T = 1 is mla_sparse_decode.  Errors: as mla_sparse_decode, with
- * MLA_ERR_SIZE for n_seq or T < 1 or n_seq*T > 4096. */
+ * T = 1 with out_bf16 = 0 is mla_sparse_decode.  Errors: as
+ * mla_sparse_decode, with MLA_ERR_SIZE for n_seq or T < 1, n_seq*T > 4096 or
+ * out_bf16 not 0 or 1. */
 int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla_bf16 *pe_cache, int S_cap,
                              const int32_t *topk_idx, int K, const int32_t *end_pos, int n_seq, int T,
-                             float softmax_scale, const mla_bf16 *wkv_b, float *out, void *workspace,
+                             float softmax_scale, const mla_bf16 *wkv_b, void *out, int out_bf16, void *workspace,
                              size_t ws_bytes, int32_t *dev_status, mla_stream_t stream);
 
 /* mla_out_up -- value up-projection alone ("Attention weights" page, excerpt
@@ -242,6 +246,26 @@ int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, float *out, mla
 int mla_cache_append(const mla_bf16 *kv_a, const float *kv_norm_w, float eps, const float *cis, int max_seq_len,
                      const int32_t *end_pos, int B, int T, mla_bf16 *kv_cache, mla_bf16 *pe_cache, int S_cap,
                      int32_t *dev_status, mla_stream_t stream);
+
+/* mla_linear_bf16 -- token-by-weight projection Y = X . W^T, the layout of
+ * the pages' Linear layers on either side of the attention ("Query heads"
+ * page, excerpt mla-init: wkv_a = Linear(dim, 576) makes the kv_a rows that
+ * mla_cache_append takes; wo = RowParallelLinear(128*128, dim); "Attention
+ * weights" page, excerpt mla-output: wo applied to the flattened head
+ * outputs).  bf16 operands, fp32 accumulation on the tensor cores:
+ *   Y[m][n] = sum_k X[m][k] * W[n][k]
+ *   x  [M][K] bf16, w [N][K] bf16 (device, 16-byte aligned, K % 8 == 0).
+ *   Exactly one of y_f32 [M][N] fp32 / y_bf16 [M][N] bf16 is non-NULL.
+ *   workspace: mla_linear_workspace_size(M, N, K) bytes of device scratch
+ *   (16-byte aligned; NULL allowed when that size is 256, i.e. no split of K
+ *   is needed on the current device).  When K is split across CTAs the
+ *   partial sums are added in a fixed order, so results are reproducible.
+ * Errors: MLA_ERR_NULL (x or w NULL, or not exactly one output),
+ * MLA_ERR_ALIGN, MLA_ERR_SIZE (M, N < 1, K < 8 or K % 8 != 0),
+ * MLA_ERR_WORKSPACE, MLA_ERR_CUDA. */
+size_t mla_linear_workspace_size(int M, int N, int K);
+int mla_linear_bf16(const mla_bf16 *x, const mla_bf16 *w, int M, int N, int K, float *y_f32, mla_bf16 *y_bf16,
+                    void *workspace, size_t ws_bytes, int32_t *dev_status, mla_stream_t stream);
 
 /* mla_weight_dequant_fp8 -- block-scaled fp8 weight to bf16 (the pages'
  * weight_dequant(wkv_b.weight, wkv_b.scale), "Rotated query part" page,

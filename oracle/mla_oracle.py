@@ -304,6 +304,21 @@ def decode_step(q_nope, q_pe, kv_cache, pe_cache, wkv_b, topk_idx, end_pos, inv_
 
 
 # --------------------------------------------------------------------------
+# Projections on either side of the attention ("Query heads" page, excerpt
+# mla-init: wkv_a = Linear(dim, 512 + 64), wo = RowParallelLinear(128 * 128,
+# dim); "Attention weights" page, excerpt mla-output: wo(x.flatten(2))).  A
+# Linear layer without bias: y = x . W^T with W stored [out, in].
+# --------------------------------------------------------------------------
+def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+
+
+def output_projection(heads: np.ndarray, wo: np.ndarray) -> np.ndarray:
+    """heads [B,128,128] flattened to [B,16384] (head-major), times wo^T."""
+    return linear(heads.reshape(heads.shape[0], -1), wo)
+
+
+# --------------------------------------------------------------------------
 # Multi-token decode: T query tokens per sequence.  The "Attention weights"
 # page notes that the causal mask is added to the selection before the
 # softmax; the plain reading for T tokens is that token s of sequence b sits at

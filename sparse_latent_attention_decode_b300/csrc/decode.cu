@@ -34,14 +34,14 @@ extern "C" size_t mla_sparse_decode_workspace_size(int B, int K) {
 
 extern "C" int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla_bf16 *pe_cache,
                                         int S_cap, const int32_t *topk_idx, int K, const int32_t *end_pos, int n_seq,
-                                        int T, float softmax_scale, const mla_bf16 *wkv_b, float *out,
+                                        int T, float softmax_scale, const mla_bf16 *wkv_b, void *out, int out_bf16,
                                         void *workspace, size_t ws_bytes, int32_t *dev_status, mla_stream_t stream) {
     if (!q_lat || !kv_cache || !pe_cache || !topk_idx || !end_pos || !out || !workspace) return MLA_ERR_NULL;
     if (!aligned16(q_lat) || !aligned16(kv_cache) || !aligned16(pe_cache) || !aligned16(topk_idx) ||
         !aligned16(out) || (wkv_b && !aligned16(wkv_b)) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MLA_ERR_ALIGN;
     if (n_seq < 1 || T < 1 || (long long)n_seq * T > 4096 || K < 1 || K > (1 << 20) || S_cap < 1 ||
-        (long long)n_seq * S_cap >= (1ll << 31))
+        (long long)n_seq * S_cap >= (1ll << 31) || (out_bf16 != 0 && out_bf16 != 1))
         return MLA_ERR_SIZE;
     const int B = n_seq * T;   // query rows
     const WsLayout L = ws_layout(B, K);
@@ -50,15 +50,18 @@ extern "C" int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *k
     char *ws = static_cast<char *>(workspace);
     // with wkv_b the latent output stays internal, as bf16 (the up-projection
     // rounds its operand to bf16 anyway); without it, o is the fp32 result
-    uint16_t *o_b16 = wkv_b ? reinterpret_cast<uint16_t *>(ws + L.o_lat) : nullptr;
+    float *out_f32 = out_bf16 ? nullptr : static_cast<float *>(out);
+    uint16_t *out_b16 = out_bf16 ? static_cast<uint16_t *>(out) : nullptr;
+    // with wkv_b the latent o goes through the workspace (bf16) to the up-projection
+    uint16_t *o_b16 = wkv_b ? reinterpret_cast<uint16_t *>(ws + L.o_lat) : out_b16;
     int launches = 0;
     int rc = launch_attn(q_lat, kv_cache, pe_cache, S_cap, topk_idx, K, end_pos, B, T, softmax_scale,
-                         wkv_b ? nullptr : out, o_b16, ws + L.attn, dev_status, s, &launches);
+                         wkv_b ? nullptr : out_f32, o_b16, ws + L.attn, dev_status, s, &launches);
     count_launches(launches);
     if (rc != MLA_OK) return rc;
     const ProfileHook &hook = profile_hook();
     const bool pdl = !(hook.start && hook.stop);
-    if (wkv_b) return launch_out_up(nullptr, o_b16, wkv_b, B, out, dev_status, s, pdl);
+    if (wkv_b) return launch_out_up(nullptr, o_b16, wkv_b, B, out_f32, out_b16, dev_status, s, pdl);
     return MLA_OK;
 }
 
@@ -67,7 +70,7 @@ extern "C" int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache
                                  float softmax_scale, const mla_bf16 *wkv_b, float *out, void *workspace,
                                  size_t ws_bytes, int32_t *dev_status, mla_stream_t stream) {
     return mla_sparse_decode_tokens(q_lat, kv_cache, pe_cache, S_cap, topk_idx, K, end_pos, B, 1, softmax_scale,
-                                    wkv_b, out, workspace, ws_bytes, dev_status, stream);
+                                    wkv_b, out, 0, workspace, ws_bytes, dev_status, stream);
 }
 
 extern "C" const char *mla_status_string(int code) {

@@ -9,9 +9,10 @@ namespace mla {
 
 // Value up-projection of the normalised latent output o, given either as
 // fp32 (o_f32, the standalone entry point) or as bf16 (o_b16, written by the
-// attention path); exactly one of them is non-NULL.
+// attention path); exactly one of them is non-NULL.  The head outputs go to
+// out (fp32) or, when out_b16 is non-NULL, to out_b16 (bf16).
 int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
-                  int32_t *status, cudaStream_t s, bool pdl);
+                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl);
 
 // Sparse attention (tensor-core kernel + split combine) over B query rows,
 // T per sequence: row b is token b % T of cache sequence b / T, at position

@@ -69,7 +69,8 @@ __device__ __forceinline__ void stage_f32(const float *__restrict__ o_lat, int h
 __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ CUtensorMap wmap,
                                                         const __grid_constant__ CUtensorMap omap,
                                                         const float *__restrict__ o_f32, bool o_is_b16, int B,
-                                                        float *__restrict__ out, int32_t *status) {
+                                                        float *__restrict__ out, uint16_t *__restrict__ out_b16,
+                                                        int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,7 +145,12 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int b = n0 + j0 + i;
-                if (b < B) out[((size_t)b * H + h) * DV + d] = __uint_as_float(v[i]);
+                if (b >= B) continue;
+                const size_t at = ((size_t)b * H + h) * DV + d;
+                if (out_b16)
+                    out_b16[at] = f2bf(__uint_as_float(v[i]));
+                else
+                    out[at] = __uint_as_float(v[i]);
             }
         }
         tc_fence_before();
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
 }  // namespace outup
 
 int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
-                  int32_t *status, cudaStream_t s, bool pdl) {
+                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl) {
     CUtensorMap wmap, omap;
     {
         const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
@@ -188,7 +194,7 @@ int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     const cudaError_t err = launch_k(pdl, outup::out_up_kernel, dim3(H), dim3(128), outup::SMEM_BYTES, s, wmap,
-                                     omap, o_f32, o_b16 != nullptr, B, out, status);
+                                     omap, o_f32, o_b16 != nullptr, B, out, out_b16, status);
     count_launches(1);
     return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -201,5 +207,5 @@ extern "C" int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, floa
     if (!o_lat || !wkv_b || !out) return MLA_ERR_NULL;
     if (!aligned16(o_lat) || !aligned16(wkv_b) || !aligned16(out)) return MLA_ERR_ALIGN;
     if (B < 1 || B > 4096) return MLA_ERR_SIZE;
-    return launch_out_up(o_lat, nullptr, wkv_b, B, out, nullptr, (cudaStream_t)stream, false);
+    return launch_out_up(o_lat, nullptr, wkv_b, B, out, nullptr, nullptr, (cudaStream_t)stream, false);
 }

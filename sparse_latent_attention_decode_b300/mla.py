@@ -58,7 +58,9 @@ def _load():
         "mla_weight_dequant_fp8": (I, [P, P, I, I, I, P, P]),
         "mla_cache_append": (I, [P, P, F, P, I, P, I, I, P, P, I, P, P]),
         "mla_absorb_q_tokens": (I, [P, P, P, I, P, P, I, I, P, P, P]),
-        "mla_sparse_decode_tokens": (I, [P, P, P, I, P, I, P, I, I, F, P, P, P, Z, P, P]),
+        "mla_sparse_decode_tokens": (I, [P, P, P, I, P, I, P, I, I, F, P, P, I, P, Z, P, P]),
+        "mla_linear_workspace_size": (Z, [I, I, I]),
+        "mla_linear_bf16": (I, [P, P, I, I, I, P, P, P, Z, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -72,7 +74,8 @@ _lib = _load()
 EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "mla_rope_apply", "mla_rope_apply_layout",
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
             "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws", "mla_weight_dequant_fp8",
-            "mla_cache_append", "mla_absorb_q_tokens", "mla_sparse_decode_tokens")
+            "mla_cache_append", "mla_absorb_q_tokens", "mla_sparse_decode_tokens",
+            "mla_linear_workspace_size", "mla_linear_bf16")
 STATIC_WS_BYTES = 32 << 20
 
 
@@ -230,10 +233,13 @@ def mla_absorb_q_tokens(q_nope, q_pe, cis, end_pos, wkv_b, out=None, dev_status=
 
 
 def mla_sparse_decode_tokens(q_lat, kv_cache, pe_cache, topk_idx, end_pos, softmax_scale, wkv_b=None, out=None,
-                             workspace=None, dev_status=None) -> torch.Tensor:
+                             workspace=None, dev_status=None, out_dtype=torch.float32) -> torch.Tensor:
     """mla_sparse_decode for T tokens per sequence: q_lat [n, T, 128, 576],
     topk_idx [n, T, K]; token s of sequence b sees its selected positions up to
-    end_pos[b] - T + s.  Returns [n, T, 128, 128] (or [n, T, 128, 512])."""
+    end_pos[b] - T + s.  Returns [n, T, 128, 128] (or [n, T, 128, 512]) in
+    out_dtype (float32 or bfloat16)."""
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
     n, T, K = topk_idx.shape
     S_cap = kv_cache.shape[1]
     _need(q_lat, "q_lat", torch.bfloat16, (n, T, N_HEADS, Q_LAT))
@@ -245,14 +251,43 @@ def mla_sparse_decode_tokens(q_lat, kv_cache, pe_cache, topk_idx, end_pos, softm
         _need(wkv_b, "wkv_b", torch.bfloat16, (N_HEADS * (D_NOPE + D_V), KV_LORA))
     width = D_V if wkv_b is not None else KV_LORA
     if out is None:
-        out = torch.empty(n, T, N_HEADS, width, dtype=torch.float32, device=q_lat.device)
-    _need(out, "out", torch.float32, (n, T, N_HEADS, width))
+        out = torch.empty(n, T, N_HEADS, width, dtype=out_dtype, device=q_lat.device)
+    _need(out, "out", out_dtype, (n, T, N_HEADS, width))
     if workspace is None:
         workspace = torch.empty(workspace_size(n * T, K), dtype=torch.uint8, device=q_lat.device)
     _check(_lib.mla_sparse_decode_tokens(_ptr(q_lat), _ptr(kv_cache), _ptr(pe_cache), S_cap, _ptr(topk_idx), K,
                                          _ptr(end_pos), n, T, float(softmax_scale), _ptr(wkv_b), _ptr(out),
+                                         1 if out_dtype == torch.bfloat16 else 0,
                                          _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                          _stream(q_lat.device)), "mla_sparse_decode_tokens")
+    return out
+
+
+def linear_workspace_size(M: int, N: int, K: int) -> int:
+    n = int(_lib.mla_linear_workspace_size(M, N, K))
+    if n == 0:
+        raise MLAError(f"linear workspace size undefined for M={M}, N={N}, K={K}")
+    return n
+
+
+def mla_linear_bf16(x, w, out_dtype=torch.float32, out=None, workspace=None, dev_status=None) -> torch.Tensor:
+    """Y = X . W^T for x [M, K] and w [N, K] (bf16), fp32 accumulation; the
+    result [M, N] is float32 or bfloat16."""
+    M, K = x.shape
+    N = w.shape[0]
+    _need(x, "x", torch.bfloat16, (M, K))
+    _need(w, "w", torch.bfloat16, (N, K))
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    _need(out, "out", out_dtype, (M, N))
+    if workspace is None:
+        workspace = torch.empty(linear_workspace_size(M, N, K), dtype=torch.uint8, device=x.device)
+    f32 = out if out_dtype == torch.float32 else None
+    b16 = out if out_dtype == torch.bfloat16 else None
+    _check(_lib.mla_linear_bf16(_ptr(x), _ptr(w), M, N, K, _ptr(f32), _ptr(b16), _ptr(workspace), workspace.numel(),
+                                _ptr(dev_status), _stream(x.device)), "mla_linear_bf16")
     return out
 
 

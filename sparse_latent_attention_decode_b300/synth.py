@@ -170,6 +170,14 @@ def make_token_inputs(wl: Workload, T: int, seed: int = 0, threads: int = 8) -> 
     return t
 
 
+def make_linear_inputs(seed: int, M: int, N: int, K: int, name: str = "linear"):
+    """Token rows x [M, K] ~ N(0, 1) and a weight w [N, K] ~ N(0, K^-1/2), both
+    bf16: the shapes of wkv_a (N = 576, K = dim) and wo (N = dim, K = 16384)."""
+    x = _randn_bf16((M, K), _gen(seed, name + "/x"))
+    w = _randn_bf16((N, K), _gen(seed, name + "/w"), std=K ** -0.5)
+    return x, w
+
+
 def make_fp8_weight(seed: int, rows: int = N_HEADS * (D_NOPE + D_V), cols: int = KV_LORA, block: int = 128,
                     name: str = "wkv_b_fp8"):
     """A block-scaled fp8 weight: e4m3 codes [rows, cols] (uint8) and fp32

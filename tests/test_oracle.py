@@ -532,3 +532,20 @@ def test_position_pin_catches_tokens_placed_at_the_last_position(monkeypatch):
     ref = O.decode_step(x["q_nope"][:, 0], x["q_pe"][:, 0], x["kv_cache"], x["pe_cache"], x["wkv_b"],
                         x["topk_idx"][:, 0], x["end_pos"] - T + 1, U_INV_FREQ, O.softmax_scale())
     assert not np.allclose(got[:, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------- projections
+def test_linear_against_loops_on_a_non_square_case():
+    rng = np.random.default_rng(8)
+    x, w = rng.standard_normal((3, 5)), rng.standard_normal((4, 5))
+    want = np.array([[sum(x[m, k] * w[n, k] for k in range(5)) for n in range(4)] for m in range(3)])
+    assert np.allclose(O.linear(x, w), want, rtol=1e-14, atol=1e-14)
+
+
+def test_output_projection_flattens_head_major():
+    heads = np.zeros((1, 128, 128))
+    heads[0, 3, 7] = 1.0                       # head 3, feature 7 -> input column 3*128 + 7
+    wo = np.zeros((5, 128 * 128))
+    wo[2, 3 * 128 + 7] = 2.5
+    wo[4, 7 * 128 + 3] = 9.0                   # the transposed position must not be picked up
+    assert np.array_equal(O.output_projection(heads, wo), [[0, 0, 2.5, 0, 0]])

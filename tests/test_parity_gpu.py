@@ -501,3 +501,69 @@ def test_multi_token_bad_end_pos_is_reported():
     torch.cuda.synchronize()
     assert int(st.item()) & mla.MLA_DEV_BAD_END_POS       # end_pos 3 < T = 4
     assert torch.all(out[0] == 0) and torch.any(out[1] != 0)
+
+
+# ----------------------------------------------------------------- projections (wkv_a, wo)
+def _assert_linear_close(got, x, w, cols=None, bf16_out=False):
+    xd, wd = synth.to_f64(x), synth.to_f64(w)
+    if cols is not None:
+        wd = wd[cols]
+        got = got[:, cols]
+    ref = O.linear(xd, wd)
+    mag = O.linear(np.abs(xd), np.abs(wd))       # sum_k |x w|: the scale of fp32 accumulation error
+    g = got.cpu().double().numpy()
+    tol = 2e-6 * mag + (2.0 ** -8 * np.abs(ref) if bf16_out else 0.0)
+    assert np.all(np.abs(g - ref) <= tol), float(np.max(np.abs(g - ref) / np.maximum(mag, 1e-30)))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 576, 7168), (64, 576, 7168), (3, 200, 72), (17, 129, 1024),
+                                   (300, 256, 128), (64, 1024, 16384), (256, 128, 64)])
+def test_linear_matches_oracle(M, N, K):
+    x, w = synth.make_linear_inputs(M * 31 + N, M, N, K)
+    got = mla.mla_linear_bf16(x.cuda(), w.cuda())
+    torch.cuda.synchronize()
+    _assert_linear_close(got, x, w)
+
+
+def test_linear_wo_full_size_sampled_columns_and_bf16_output():
+    M, N, K = 64, 7168, 16384
+    x, w = synth.make_linear_inputs(61, M, N, K)
+    dx, dw = x.cuda(), w.cuda()
+    y = mla.mla_linear_bf16(dx, dw)
+    yb = mla.mla_linear_bf16(dx, dw, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    cols = np.random.default_rng(0).choice(N, 384, replace=False)
+    cols = np.concatenate([cols, [0, 127, 128, N - 1]])
+    _assert_linear_close(y, x, w, cols)
+    _assert_linear_close(yb, x, w, cols, bf16_out=True)
+    assert torch.equal(yb, y.to(torch.bfloat16))     # one rounding of the same fp32 sums
+    assert torch.equal(y, mla.mla_linear_bf16(dx, dw))   # reproducible
+
+
+def test_decode_bf16_output_feeds_the_output_projection():
+    B, K, dim = 4, 256, 1024
+    t = synth.make_inputs(synth.small_workload(B, [500, 256, 1000, 3], k=K, K=K, S_cap=1024), seed=67)
+    d = _dev(t)
+    cis = mla.rope_freqs_init()
+    q_lat = mla.mla_absorb_q(d["q_nope"], d["q_pe"], cis, d["end_pos"], d["wkv_b"])
+    out32 = mla.mla_sparse_decode_tokens(q_lat[:, None], d["kv_cache"], d["pe_cache"], d["topk_idx"][:, None],
+                                         d["end_pos"], U.SCALE, wkv_b=d["wkv_b"])
+    out16 = mla.mla_sparse_decode_tokens(q_lat[:, None], d["kv_cache"], d["pe_cache"], d["topk_idx"][:, None],
+                                         d["end_pos"], U.SCALE, wkv_b=d["wkv_b"], out_dtype=torch.bfloat16)
+    o16 = mla.mla_sparse_decode_tokens(q_lat[:, None], d["kv_cache"], d["pe_cache"], d["topk_idx"][:, None],
+                                       d["end_pos"], U.SCALE, out_dtype=torch.bfloat16)
+    o32 = mla.mla_sparse_decode(q_lat, d["kv_cache"], d["pe_cache"], d["topk_idx"], d["end_pos"], U.SCALE)
+    _, wo = synth.make_linear_inputs(68, 1, dim, 128 * 128, name="wo")
+    y = mla.mla_linear_bf16(out16.reshape(B, -1), wo.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    # the latent o in bf16 is the attention's own bf16 rounding (the combine or the epilogue)
+    assert torch.allclose(o16[:, 0].float(), o32, rtol=2 ** -8, atol=1e-6)
+    x = U.oracle_inputs(t)
+    heads = U.oracle_out(x, list(range(B)))
+    ora = O.output_projection(O.round_to_bf16(heads), synth.to_f64(wo))
+    mag = O.output_projection(np.abs(heads), np.abs(synth.to_f64(wo)))
+    err = np.abs(y.cpu().double().numpy() - ora)
+    # the head outputs carry the attention tolerance (relative to their size)
+    # before the projection; the projection adds fp32 accumulation error
+    assert np.all(err <= 5e-3 * mag + 1e-4), float(np.max(err / np.maximum(mag, 1e-30)))
