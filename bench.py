@@ -424,9 +424,9 @@ def run_ours(args):
     e2e_ms = max_over_ranks(statistics.mean(et[2 * i].elapsed_time(et[2 * i + 1]) for i in range(args.steps)),
                             world, dev)
 
-    next_rows = measure_next_rows(mla, synth, dev, flush, args.seed)
+    next_rows = measure_next_rows(mla, synth, dev, flush, args.seed, n=args.next_steps)
     if B % 2 == 0:
-        next_rows["multi_token_decode"] = measure_multi_token(mla, step, d, B, K, rows, flush)
+        next_rows["multi_token_decode"] = measure_multi_token(mla, step, d, B, K, rows, flush, n=args.next_steps)
 
     if rank != 0:
         return None
@@ -508,6 +508,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--kernel-steps", type=int, default=200,
                     help="extra steps in which the attention kernel alone is timed")
+    ap.add_argument("--next-steps", type=int, default=50,
+                    help="timed launches per added entry point (next_rows)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--seed", type=int, default=0)

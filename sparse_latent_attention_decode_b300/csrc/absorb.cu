@@ -22,10 +22,13 @@ namespace absorb {
 
 using namespace tc;
 
-constexpr int NMAX = 128;                      // sequences per pass
+constexpr int NMAX = 128;                      // sequences per pass, at most
 constexpr int A_BOX = 128 * 128;               // one [128 d][64 c] box of W_UK, bytes
-constexpr int B_BOX = NMAX * 128;              // one [128 b][64 d] box of q_nope, bytes
+constexpr int B_BOX = NMAX * 128;              // one [128 b][64 d] box of q_nope, bytes, at most
 constexpr int SMEM_BYTES = 2 * A_BOX + 2 * B_BOX + 1024;
+// Shared memory for `nmax` sequences per pass: with B <= 64 four CTAs fit on
+// an SM, so the 512 CTAs run as one wave.
+__host__ __device__ constexpr int smem_bytes(int nmax) { return 2 * A_BOX + 2 * nmax * 128 + 1024; }
 constexpr int PAIRS_PER_TILE = NPAIR / 4;      // rotary pairs handled by each latent tile
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
@@ -77,7 +80,8 @@ __device__ __forceinline__ void rope_part(const uint16_t *__restrict__ q_pe, con
 __global__ void __launch_bounds__(128)
     absorb_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
                   const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis, int max_seq_len,
-                  const int32_t *__restrict__ end_pos, int B, int T, uint16_t *__restrict__ q_lat, int32_t *status) {
+                  const int32_t *__restrict__ end_pos, int B, int T, int nmax, uint16_t *__restrict__ q_lat,
+                  int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -110,15 +114,16 @@ __global__ void __launch_bounds__(128)
         tma_load_2d(smem_u32(sA + A_BOX), &wmap, 128 * t + 64, h * WROWS, &bars.a_full);
     }
 
-    const int npass = (B + NMAX - 1) / NMAX;
+    const int bbox = nmax * 128;   // bytes of one [nmax b][64 d] box of q_nope
+    const int npass = (B + nmax - 1) / nmax;
     for (int pass = 0; pass < npass && ok; ++pass) {
-        const int n0 = pass * NMAX;
-        const int nb = min(NMAX, B - n0);
+        const int n0 = pass * nmax;
+        const int nb = min(nmax, B - n0);
         const int N = (nb + 15) & ~15;
         if (tid == 0) {
-            mbar_expect_tx(&bars.b_full, 2 * B_BOX);
+            mbar_expect_tx(&bars.b_full, 2 * bbox);
             tma_load_3d(smem_u32(sB), &qmap, 0, h, n0, &bars.b_full);
-            tma_load_3d(smem_u32(sB + B_BOX), &qmap, 64, h, n0, &bars.b_full);
+            tma_load_3d(smem_u32(sB + bbox), &qmap, 64, h, n0, &bars.b_full);
         }
         if (pass == 0) rope_part(q_pe, cis, max_seq_len, end_pos, B, T, h, t, q_lat, status, tid);
         if (tid == 0) {
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t ad = smem_desc(smem_u32(sA) + kk * 2048, A_BOX, 1024, 2);
-                    const uint64_t bd = smem_desc(smem_u32(sB + (kk >> 2) * B_BOX) + (kk & 3) * 32, 16, 1024, 2);
+                    const uint64_t bd = smem_desc(smem_u32(sB + (kk >> 2) * bbox) + (kk & 3) * 32, 16, 1024, 2);
                     mma_ss(tmem, ad, bd, idesc, kk > 0);
                 }
                 mma_commit(&bars.mma_done);
@@ -180,6 +185,7 @@ extern "C" int mla_absorb_q_tokens(const mla_bf16 *q_nope, const mla_bf16 *q_pe,
         return MLA_ERR_ALIGN;
     if (n_seq < 1 || T < 1 || (long long)n_seq * T > 4096 || max_seq_len < 1) return MLA_ERR_SIZE;
     const int B = n_seq * T;   // query rows
+    const int nmax = B >= absorb::NMAX ? absorb::NMAX : (B + 15) / 16 * 16;
     CUtensorMap wmap, qmap;
     {
         const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
@@ -190,7 +196,7 @@ extern "C" int mla_absorb_q_tokens(const mla_bf16 *q_nope, const mla_bf16 *q_pe,
     {
         const uint64_t dims[3] = {(uint64_t)DN, (uint64_t)H, (uint64_t)B};
         const uint64_t strides[2] = {(uint64_t)DN * 2, (uint64_t)H * DN * 2};
-        const uint32_t box[3] = {64, 1, absorb::NMAX};
+        const uint32_t box[3] = {64, 1, (uint32_t)nmax};
         if (!make_tmap_bf16(&qmap, q_nope, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
     }
     cudaStream_t s = (cudaStream_t)stream;
@@ -203,8 +209,8 @@ extern "C" int mla_absorb_q_tokens(const mla_bf16 *q_nope, const mla_bf16 *q_pe,
             return MLA_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    absorb::absorb_kernel<<<dim3(4, H), 128, absorb::SMEM_BYTES, s>>>(
-        wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, T, q_lat, dev_status);
+    absorb::absorb_kernel<<<dim3(4, H), 128, absorb::smem_bytes(nmax), s>>>(
+        wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, T, nmax, q_lat, dev_status);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
