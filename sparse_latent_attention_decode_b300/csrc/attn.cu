@@ -15,9 +15,11 @@
 //         latent part of Q_r in TMEM and 2 with its rotary part in shared
 //         memory; B = the gathered tile, K-major.
 //   The two partial score tiles are exchanged through distributed shared
-//   memory (raw scores as fp16, st.async into a ring of three receive
-//   buffers whose mbarriers count the arriving bytes) and summed: both CTAs
-//   then hold the full scores and run the same online softmax.
+//   memory and summed: each softmax warpgroup writes its CTA's raw scores as
+//   fp16 into a send buffer, and a copy warp ships the 16 KB with one bulk
+//   copy into a ring of three receive buffers in the peer, whose mbarriers
+//   count the arriving bytes.  Both CTAs then hold the full scores and run
+//   the same online softmax.
 //   PV  : O_r[128 heads, 256 latent] += P[128, 64] . V_r[64, 256]  (A = P
 //         as bf16 in shared memory, B = the same gathered tile read MN-major).
 // TMEM per CTA: O_r columns [0,256), latent Q_r [256,384), two score
@@ -34,9 +36,12 @@
 //   warp 8      issues QK(j) once stage j is full and score buffer j%2 has
 //               been read (block j-2);
 //   warp 9      issues PV(j) once P(j) is in shared memory;
+//   warp 10     copies block j's partial scores to the peer once they are in
+//               the send buffer, and frees the buffer when the copy has read it;
 //   warps 12-15 softmax of the even blocks, warps 16-19 of the odd blocks
 //               (ping-pong): one thread per head, all 64 keys of its block.
-// The selection of the unit is staged in shared memory once (positions
+// The selection of the unit (at most 2048 entries; longer selections are
+// split across units) is staged in shared memory once (positions
 // outside [0, end_pos) become -1), so no global index load sits on the
 // per-block path.
 //
@@ -72,15 +77,16 @@ constexpr int STAGE_PE = NK * 64;            // 32 rotary columns x 64 keys (64B
 constexpr int STAGE = STAGE_KV + STAGE_PE;   // 36864
 constexpr int NRECV = 3;                     // exchange ring depth
 constexpr int RECV = H * NK * 2;             // fp16 partial scores of the peer, 128 x 64
-constexpr int IDX_CAP = 4096;                // selection entries of one unit staged in shared memory
+constexpr int IDX_CAP = 2048;                // selection entries of one unit staged in shared memory
 constexpr int QROPE = H * 64;                // rotary part of Q_r: 128 heads x 32 bf16 (64B swizzle)
-constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_CAP * 4 + 1024;
+constexpr int SEND = RECV;                   // this CTA's partial scores of one block, shipped by bulk copy
+constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_CAP * 4 + SEND + 1024;
 constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 384, TMEM_COLS = 512;   // S buffer k at S_COL + 64 k
 constexpr int THREADS = 640;
 constexpr int GATHER_THREADS = 256;          // warps 0-7
 constexpr int CPT = NK * 36 / GATHER_THREADS;   // 9 chunks per gather thread per block
 static_assert(CPT * GATHER_THREADS == NK * 36, "chunks must divide evenly");
-constexpr int QK_WARP = 8, PV_WARP = 9;
+constexpr int QK_WARP = 8, PV_WARP = 9, COPY_WARP = 10;
 constexpr int SOFTMAX_WARP0 = 12;            // warps 12-19: two warpgroups
 constexpr int WG_THREADS = 128;
 // registers per thread after reallocation: 256*72 + 128*56 + 256*136 <= 640*96
@@ -111,10 +117,11 @@ struct Bars {
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_ready;
     uint64_t recv_full[NRECV];
     uint64_t m_ready[2];   // m after block j is in mval[j % 2]
-    uint64_t l_ready;      // both running sums are in lsum
+    uint64_t l_ready;      // both running sums are in lsum (the send buffer, after the last copy)
+    uint64_t send_ready;   // the send buffer holds block j's partial scores
+    uint64_t send_free;    // the copy of block j has read the send buffer
     uint32_t tmem_base;
     float mval[2][H];
-    float lsum[2][H];
 };
 
 __device__ __forceinline__ void fail(const Params &p) { report(p.status, MLA_DEV_TIMEOUT); }
@@ -134,6 +141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     uint8_t *recv = smem + NS * STAGE;
     uint8_t *qrope = recv + NRECV * RECV;
     int32_t *sidx = reinterpret_cast<int32_t *>(qrope + QROPE);
+    uint8_t *sendbuf = qrope + QROPE + IDX_CAP * 4;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t r = cluster_rank(), peer = r ^ 1u;
@@ -174,6 +182,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         }
         mbar_init(&bars.q_ready, 2 * WG_THREADS);
         mbar_init(&bars.l_ready, 2 * WG_THREADS);
+        mbar_init(&bars.send_ready, WG_THREADS);
+        mbar_init(&bars.send_free, 1);
         for (int k = 0; k < NRECV; ++k) mbar_init(&bars.recv_full[k], 1);
         fence_mbar_init();
     }
@@ -287,6 +297,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             }
             if (!ok) fail(p);
         }
+        if (lane == 0 && nblk > 0 && warp == COPY_WARP) {
+            // ships each block's partial scores to the peer's receive slot
+            const uint32_t recv_peer = map_peer(smem_u32(recv), peer);
+            const uint32_t src = smem_u32(sendbuf);
+            for (int j = 0; j < nblk; ++j) {
+                if (!wait_until(&bars.send_ready, j & 1, deadline)) {
+                    fail(p);
+                    break;
+                }
+                const int kb = j % NRECV;
+                bulk_s2cluster(recv_peer + kb * RECV, src, SEND, map_peer(smem_u32(&bars.recv_full[kb]), peer));
+                bulk_commit();
+                bulk_wait_read();
+                mbar_arrive(&bars.send_free);
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax warpgroups (ping-pong)
         // warpgroup w handles blocks j = w, w+2, ...; thread = head h, all 64 keys
@@ -322,7 +348,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             mbar_arrive(&bars.q_ready);
         }
         const uint32_t recv_local = smem_u32(recv);
-        const uint32_t recv_peer = map_peer(recv_local, peer);
         const float sl2 = p.scale_log2;
         float m_mine = -INFINITY;   // m after this warpgroup's previous block
         float l = 0.f;              // this warpgroup's running sum, relative to m_mine
@@ -364,13 +389,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             }
             {
                 const int kb = j % NRECV;
-                const uint32_t dst = recv_peer + kb * RECV + h * 128;
-                const uint32_t cbar = map_peer(smem_u32(&bars.recv_full[kb]), peer);
+                // this CTA's partial scores go to the send buffer (free once the copy of
+                // block j-1 has read it); the copy warp ships them to the peer's slot
+                if (j >= 1 && !warp_wait(&bars.send_free, (j - 1) & 1, deadline)) { ok = false; break; }
+                const uint32_t sb = smem_u32(sendbuf) + h * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_async_v4(dst + ((c ^ (h & 7)) << 4), pack_f16_sat(x[8 * c], x[8 * c + 1]),
-                                pack_f16_sat(x[8 * c + 2], x[8 * c + 3]), pack_f16_sat(x[8 * c + 4], x[8 * c + 5]),
-                                pack_f16_sat(x[8 * c + 6], x[8 * c + 7]), cbar);
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t a0 = pack_f16_sat(x[8 * c], x[8 * c + 1]), a1 = pack_f16_sat(x[8 * c + 2], x[8 * c + 3]);
+                    const uint32_t a2 = pack_f16_sat(x[8 * c + 4], x[8 * c + 5]), a3 = pack_f16_sat(x[8 * c + 6], x[8 * c + 7]);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sb + ((c ^ (h & 7)) << 4)), "r"(a0), "r"(a1),
+                                 "r"(a2), "r"(a3)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars.send_ready);
                 // receive the peer's half of block j: this warpgroup announces the bytes
                 if (wtid == 0) mbar_expect_tx(&bars.recv_full[kb], RECV);
                 if (!warp_wait(&bars.recv_full[kb], (j / NRECV) & 1, deadline)) { ok = false; break; }
@@ -471,10 +503,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             if (ok) {
                 m_fin = bars.mval[jl & 1][h];
                 const float lw = (m_mine == -INFINITY || m_fin == -INFINITY) ? 0.f : l * ex2(m_mine - m_fin);
-                bars.lsum[w][h] = lw;
+                // the sums go to the send buffer once the last copy has read it
+                float *lsum = reinterpret_cast<float *>(sendbuf);
+                if (!warp_wait(&bars.send_free, jl & 1, deadline)) ok = false;
+                lsum[w * H + h] = lw;
                 mbar_arrive(&bars.l_ready);
                 if (!warp_wait(&bars.l_ready, 0, deadline)) ok = false;
-                lt = bars.lsum[0][h] + bars.lsum[1][h];
+                lt = lsum[h] + lsum[H + h];
                 if (ok && !warp_wait(&bars.pv_done[jl & 1], (jl >> 1) & 1, deadline)) ok = false;
                 tc_fence_after();
             }

@@ -296,6 +296,19 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
+// shared memory of a CTA of the cluster; the destination mbarrier (in that
+// CTA, cluster address) counts the bytes.  The source may be reused after
+// bulk_wait_read() by the issuing thread.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_caddr, uint32_t src, uint32_t bytes, uint32_t cbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_caddr),
+                 "r"(src), "r"(bytes), "r"(cbar)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // ------------------------------------------------------------ programmatic dependent launch
 // Wait until the grids this one depends on have completed and their memory is visible.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
