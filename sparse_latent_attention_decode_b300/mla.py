@@ -472,3 +472,62 @@ class HostDecodeStep(DecodeStep):
         out = self(self.d_q_nope, self.d_q_pe, kv_cache, pe_cache, wkv_b, self.d_topk, self.d_end)
         self.h_out.copy_(out, non_blocking=True)
         return self.h_out
+
+
+class HostDecodePipeline:
+    """Decode steps from pinned host buffers with the transfers overlapped:
+    the inputs of step i go up on one copy stream and the outputs of step i-1
+    come back on another while the device computes.  Two device buffer sets
+    alternate; every step still copies its own inputs in and its own head
+    outputs out.  ``submit`` enqueues one step and returns at once; read an
+    output buffer only after ``finish`` (or after the step two submissions
+    later has been submitted and ``finish`` has run)."""
+
+    def __init__(self, B: int, K: int, device="cuda", params: RopeParams | None = None):
+        self.device = torch.device(device)
+        self.steps = [HostDecodeStep(B, K, self.device, params) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(self.device)
+        self.d2h = torch.cuda.Stream(self.device)
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.copied_out = [torch.cuda.Event() for _ in range(2)]
+        self.count = 0
+
+    def h2d_bytes(self):
+        return self.steps[0].h2d_bytes()
+
+    def d2h_bytes(self):
+        return self.steps[0].d2h_bytes()
+
+    def submit(self, h_q_nope, h_q_pe, h_topk, h_end, kv_cache, pe_cache, wkv_b, h_out):
+        i, k = self.count, self.count % 2
+        st = self.steps[k]
+        compute = torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(self.h2d):
+            if i >= 2:
+                self.h2d.wait_event(self.computed[k])      # step i-2 has read these device inputs
+            st.d_q_nope.copy_(h_q_nope, non_blocking=True)
+            st.d_q_pe.copy_(h_q_pe, non_blocking=True)
+            st.d_topk.copy_(h_topk, non_blocking=True)
+            st.d_end.copy_(h_end, non_blocking=True)
+            self.in_ready[k].record(self.h2d)
+        compute.wait_event(self.in_ready[k])
+        if i >= 2:
+            compute.wait_event(self.copied_out[k])          # step i-2's outputs have left the device buffer
+        out = st(st.d_q_nope, st.d_q_pe, kv_cache, pe_cache, wkv_b, st.d_topk, st.d_end)
+        self.computed[k].record(compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.computed[k])
+            h_out.copy_(out, non_blocking=True)
+            self.copied_out[k].record(self.d2h)
+        self.count += 1
+
+    def finish(self):
+        """Make the current stream wait for every submitted step's copies."""
+        compute = torch.cuda.current_stream(self.device)
+        for k in range(min(self.count, 2)):
+            compute.wait_event(self.copied_out[k])
+
+    def check_status(self):
+        for st in self.steps:
+            st.check_status()

@@ -569,3 +569,54 @@ def test_decode_bf16_output_feeds_the_output_projection():
     # the head outputs carry the attention tolerance (relative to their size)
     # before the projection; the projection adds fp32 accumulation error
     assert np.all(err <= 5e-3 * mag + 1e-4), float(np.max(err / np.maximum(mag, 1e-30)))
+
+
+def test_host_buffer_step_matches_oracle_eager_and_captured():
+    # the end-to-end path bench.py times: pinned host inputs in, head outputs back
+    B, K = 3, 256
+    t = synth.make_inputs(synth.small_workload(B, [700, 256, 1000], k=K, K=K, S_cap=1024), seed=71)
+    d = _dev(t)
+    h = {k: t[k].pin_memory() for k in ("q_nope", "q_pe", "topk_idx", "end_pos")}
+    hs = mla.HostDecodeStep(B, K)
+    out = hs.run(h["q_nope"], h["q_pe"], h["topk_idx"], h["end_pos"], d["kv_cache"], d["pe_cache"], d["wkv_b"])
+    torch.cuda.synchronize()
+    hs.check_status()
+    assert out.device.type == "cpu" and out.is_pinned()
+    x = U.oracle_inputs(t)
+    U.assert_attn_close(out.numpy(), U.oracle_out(x, list(range(B))), "host-buffer step")
+    eager = out.clone()
+    g = mla.CapturedStep(hs.run, h["q_nope"], h["q_pe"], h["topk_idx"], h["end_pos"], d["kv_cache"],
+                         d["pe_cache"], d["wkv_b"])
+    h["q_nope"].mul_(-1)                      # new inputs in the captured host buffers
+    g()
+    torch.cuda.synchronize()                  # the result is copied back asynchronously
+    got = g.out.clone()
+    x["q_nope"] = -x["q_nope"]
+    U.assert_attn_close(got.numpy(), U.oracle_out(x, list(range(B))), "captured host-buffer step")
+    h["q_nope"].mul_(-1)
+    g()
+    torch.cuda.synchronize()
+    assert torch.equal(g.out, eager)
+
+
+def test_host_pipeline_steps_each_match_their_inputs():
+    B, K, n = 2, 128, 5
+    t = synth.make_inputs(synth.small_workload(B, [400, 300], k=K, K=K, S_cap=512), seed=73)
+    d = _dev(t)
+    pipe = mla.HostDecodePipeline(B, K)
+    ins, outs, keep = [], [], []                 # keep: the pinned inputs stay alive until finish()
+    hp, ht, he = t["q_pe"].pin_memory(), t["topk_idx"].pin_memory(), t["end_pos"].pin_memory()
+    for i in range(n):
+        f = float(i + 1) * (-1) ** i              # a different query per step
+        q = (t["q_nope"].float() * f).to(torch.bfloat16)
+        ins.append(q)
+        keep.append(q.pin_memory())
+        outs.append(torch.empty(B, 128, 128, dtype=torch.float32).pin_memory())
+        pipe.submit(keep[-1], hp, ht, he, d["kv_cache"], d["pe_cache"], d["wkv_b"], outs[-1])
+    pipe.finish()
+    torch.cuda.synchronize()
+    pipe.check_status()
+    x = U.oracle_inputs(t)
+    for i in range(n):
+        x["q_nope"] = synth.to_f64(ins[i])
+        U.assert_attn_close(outs[i].numpy(), U.oracle_out(x, list(range(B))), f"pipeline step {i}")
