@@ -30,6 +30,13 @@
  *  - Return value: MLA_OK (0) on success; a negative MLA_ERR_* code when an
  *    argument check fails on the host (nothing is enqueued then), or
  *    MLA_ERR_CUDA when a launch fails.  No exception crosses the ABI.
+ *  - Kernels are chained on the stream by programmatic dependent launch.
+ *    The attention kernel starts gathering kv_cache / pe_cache rows (per
+ *    topk_idx and end_pos) while the grid before it may still be running; it
+ *    waits for that grid before reading q_lat or writing any output.  These
+ *    four inputs must therefore be complete before the call is enqueued (any
+ *    ordinary kernel, copy or event before it guarantees that); only a kernel
+ *    that itself triggers dependent launch early could break this.
  *  - Conditions only the device can see (an end_pos outside [1, S_cap], a
  *    position outside the rotary table, a bounded wait that ran out) are OR-ed
  *    as MLA_DEV_* bits into *dev_status (when dev_status is non-NULL); read it

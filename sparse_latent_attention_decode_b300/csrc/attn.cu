@@ -145,10 +145,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t r = cluster_rank(), peer = r ^ 1u;
-    // Launched as a programmatic dependent of the preceding grid: nothing an
-    // earlier grid may have written (q_lat, the caches, the selection) is read
-    // before it has completed.
-    grid_dep_wait();
+    // Launched as a programmatic dependent of the preceding grid (the query
+    // absorption): the caches, the selection and end_pos are inputs of the
+    // step, so the selection is staged and the gather starts at once; q_lat,
+    // which that grid writes, is read only by the softmax warpgroups, after
+    // their griddepcontrol.wait.
     const int unit = blockIdx.x >> 1;
     const int b = unit / p.n_split, split = unit % p.n_split;   // query row
     const int cb = b / p.T;                                     // its sequence in the caches
@@ -194,9 +195,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     tc_fence_before();
     cluster_sync();   // barriers of both CTAs initialised, TMEM address published, selection staged
     tc_fence_after();
-    // The dependent grid (value up-projection) may start its prologue now.
-    // This comes after grid_dep_wait, so every grid before this one has
-    // completed once a dependent of this grid runs.
+    // The dependent grid (value up-projection) may start its prologue now; it
+    // reads this grid's output only after its own griddepcontrol.wait, which
+    // returns once this grid -- and so the grid before it -- has completed.
     if (tid == 0) grid_dep_launch();
     const uint32_t tmem = bars.tmem_base;
     const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
@@ -323,6 +324,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         const int wtid = (warp - SOFTMAX_WARP0 - 4 * w) * 32 + lane;   // 0..127 within the warpgroup
         const uint32_t trow = tmem + (uint32_t(32 * quad) << 16);
         bool ok = true;
+        // q_lat comes from the preceding grid, and an earlier grid may still read
+        // the buffers the epilogue writes: both wait for it to complete
+        grid_dep_wait();
         if (nblk > 0) {
             // Q_r: latent [256r, 256r+256) -> TMEM as 128 bf16 pairs (warpgroup w
             // stores 16-column groups 4w .. 4w+3); rotary [32r, 32r+32) -> shared
