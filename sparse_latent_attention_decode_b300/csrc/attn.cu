@@ -119,12 +119,29 @@ struct Bars {
     uint64_t m_ready[2];   // m after block j is in mval[j % 2]
     uint64_t l_ready;      // both running sums are in lsum (the send buffer, after the last copy)
     uint64_t send_ready;   // the send buffer holds block j's partial scores
-    uint64_t send_free;    // the copy of block j has read the send buffer
+    int send_done;         // copies 0 .. send_done-1 have read the send buffer (a counter, not a
+                           // barrier: the warpgroup of block j waits for the copy of block j-1
+                           // without having seen the copy of block j-2 complete)
     uint32_t tmem_base;
     float mval[2][H];
 };
 
 __device__ __forceinline__ void fail(const Params &p) { report(p.status, MLA_DEV_TIMEOUT); }
+
+// Bounded wait until a shared-memory counter written by another thread of the
+// CTA reaches `target` (warp-uniform result).
+__device__ __forceinline__ bool wait_count(const int *counter, int target, uint64_t deadline) {
+    bool ok = true;
+    for (uint32_t i = 0; *reinterpret_cast<const volatile int *>(counter) < target; ++i) {
+        if (i >= 2) __nanosleep(32);
+        if ((i & 31) == 31 && globaltimer_ns() > deadline) {
+            ok = false;
+            break;
+        }
+    }
+    __threadfence_block();
+    return __all_sync(0xffffffffu, ok);
+}
 
 // warp-uniform bounded waits: every lane of the warp takes the same branch afterwards
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t deadline) {
@@ -184,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         mbar_init(&bars.q_ready, 2 * WG_THREADS);
         mbar_init(&bars.l_ready, 2 * WG_THREADS);
         mbar_init(&bars.send_ready, WG_THREADS);
-        mbar_init(&bars.send_free, 1);
+        bars.send_done = 0;
         for (int k = 0; k < NRECV; ++k) mbar_init(&bars.recv_full[k], 1);
         fence_mbar_init();
     }
@@ -311,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 bulk_s2cluster(recv_peer + kb * RECV, src, SEND, map_peer(smem_u32(&bars.recv_full[kb]), peer));
                 bulk_commit();
                 bulk_wait_read();
-                mbar_arrive(&bars.send_free);
+                *reinterpret_cast<volatile int *>(&bars.send_done) = j + 1;
             }
         }
     } else {
@@ -395,7 +412,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 const int kb = j % NRECV;
                 // this CTA's partial scores go to the send buffer (free once the copy of
                 // block j-1 has read it); the copy warp ships them to the peer's slot
-                if (j >= 1 && !warp_wait(&bars.send_free, (j - 1) & 1, deadline)) { ok = false; break; }
+                if (!wait_count(&bars.send_done, j, deadline)) { ok = false; break; }
                 const uint32_t sb = smem_u32(sendbuf) + h * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -509,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 const float lw = (m_mine == -INFINITY || m_fin == -INFINITY) ? 0.f : l * ex2(m_mine - m_fin);
                 // the sums go to the send buffer once the last copy has read it
                 float *lsum = reinterpret_cast<float *>(sendbuf);
-                if (!warp_wait(&bars.send_free, jl & 1, deadline)) ok = false;
+                if (!wait_count(&bars.send_done, nblk, deadline)) ok = false;
                 lsum[w * H + h] = lw;
                 mbar_arrive(&bars.l_ready);
                 if (!warp_wait(&bars.l_ready, 0, deadline)) ok = false;
