@@ -166,6 +166,24 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- helpers
+def read_stream_gbs(dev, n_bytes: int = 2 << 30, reps: int = 10) -> float:
+    """Read-only HBM stream for context beside the copy peak (which counts read
+    and write bytes): PyTorch's sum over a 2 GiB buffer, mean of `reps` runs."""
+    x = torch.ones(n_bytes // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        x.sum()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        x.sum()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    del x
+    return n_bytes / (ms * 1e-3) / 1e9
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -385,6 +403,7 @@ def run_ours(args):
     step_ms = [st[2 * i].elapsed_time(st[2 * i + 1]) for i in range(args.steps)]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, dev)
+    ms_median = statistics.median(step_ms)
 
     # ---- the attention kernel alone: CUDA events recorded by the library on
     # the launching stream right before and after it (these steps are not the
@@ -441,6 +460,10 @@ def run_ours(args):
     hbm = float(hbm) if hbm else FALLBACK_HBM_GBS
     alg_bytes = rows * ROW_BYTES
     achieved = alg_bytes / (kern * 1e-3) / 1e9
+    read_peak = read_stream_gbs(dev)
+    # the whole step's ideal time: the gathered rows plus one read of wkv_b
+    step_bytes = alg_bytes + d["wkv_b"].numel() * 2
+    step_ideal_ms = step_bytes / (hbm * 1e9) * 1e3
     traffic = traffic_record()
 
     cpu = None
@@ -453,7 +476,8 @@ def run_ours(args):
 
     line = {
         "metric": METRIC, "value": world * B / (ms_max * 1e-3), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "ms_per_step_median": ms_median,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "batch_per_gpu": B, "global_batch": world * B,
                    "end_pos": (wl.end_pos[0] if len(set(wl.end_pos)) == 1 else
@@ -468,7 +492,10 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "mla_sparse_decode attention kernel",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
-                     "alg_bytes_per_launch": alg_bytes, "kernel_ms": kern},
+                     "alg_bytes_per_launch": alg_bytes, "kernel_ms": kern,
+                     "read_stream_gbs": read_peak, "frac_of_read_stream": achieved / read_peak},
+        "step_roofline": {"bytes": step_bytes, "ideal_ms": step_ideal_ms, "frac": step_ideal_ms / ms_max,
+                          "note": "gathered rows x 1152 B + one read of wkv_b, at the copy peak"},
         "cpu_baseline": cpu,
         "next_rows": {k: dict(v, frac=v["achieved_gbs"] / hbm) for k, v in next_rows.items()},
         "clocks": clk,
