@@ -205,8 +205,10 @@ def softmax_scale(qk_head_dim: int = D_QK, max_seq_len: int = 16384, original_se
 # --------------------------------------------------------------------------
 def split_wkv_b(wkv_b: np.ndarray):
     """wkv_b [H*256, 512] viewed [H, 256, 512]: rows 0..127 of each head are the
-    key half W_UK, rows 128..255 the value half W_UV."""
-    w = wkv_b.reshape(N_HEADS, D_NOPE + D_V, KV_LORA)
+    key half W_UK, rows 128..255 the value half W_UV.  H follows the array (the
+    step is independent per head, so a block of consecutive heads is a valid
+    input)."""
+    w = wkv_b.reshape(-1, D_NOPE + D_V, KV_LORA)
     return w[:, :D_NOPE, :], w[:, D_NOPE:, :]
 
 
