@@ -620,3 +620,22 @@ def test_host_pipeline_steps_each_match_their_inputs():
     for i in range(n):
         x["q_nope"] = synth.to_f64(ins[i])
         U.assert_attn_close(outs[i].numpy(), U.oracle_out(x, list(range(B))), f"pipeline step {i}")
+
+
+def test_maximum_batch_of_query_rows():
+    # B = 4096 query rows (the ABI's limit): absorption and up-projection take
+    # 32 passes of 128 sequences, the attention grid 8192 CTAs; short caches
+    B, S, K = 4096, 64, 64
+    t = synth.make_inputs(synth.small_workload(B, [1 + (37 * b) % 64 for b in range(B)], k=40, K=K, S_cap=S),
+                          seed=83, threads=16)
+    d = _dev(t)
+    step = mla.DecodeStep(B, K)
+    out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    torch.cuda.synchronize()
+    step.check_status()
+    got = out.cpu().numpy()
+    x = U.oracle_inputs(t)
+    bs = [0, 1, 127, 128, 129, 2047, 2048, 4094, 4095] + list(range(1000, 4096, 331))
+    U.assert_attn_close(got[bs], U.oracle_out(x, bs), "B=4096 sampled sequences")
+    with pytest.raises(mla.MLAError):
+        mla.DecodeStep(B + 1, K)                # one row past the limit: no workspace size
