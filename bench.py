@@ -1,25 +1,38 @@
 #!/usr/bin/env python
 """Benchmark of one decode step of absorbed, top-k-sparse latent attention.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--configs all|none|NAME,...] [--impl ours|reference]
 
 A step is the whole path for one batch: RoPE + key absorption
 (mla_absorb_q), then scores / softmax / PV / value up-projection
 (mla_sparse_decode with wkv_b).  Inputs are seeded synthetic tensors already
 resident in HBM; the step is captured once in a CUDA graph and each timed
-step is one replay; L2 is flushed (a 256 MiB write) before every timed step
-and each step is timed with its own CUDA events on the launching stream.
+step is one replay.  Before every timed step L2 is flushed: a 256 MiB buffer
+is written, then a second 256 MiB buffer is read, so that L2 holds no line of
+the step's data and no dirty line of the flush is written back while the step
+runs.  Each step is timed with its own CUDA events on the launching stream.
 
-With N > 1 (torchrun, one process per GPU) each rank runs an independent
-replica on its own batch (different seed): no collective on the data path,
-weak scaling; a barrier and a max-over-ranks reduction bracket the timing.
+The headline line is the workload named by --workload (B=64, 16384 cached
+positions, top-2048); its ``configs`` object carries the same measurement
+for every named workload (the pages' P=1000 example at B=1, B=32 at 4096
+positions, B=64 at 16384, the ragged B=128 batch, dense B=16 and dense B=1),
+each with the attention kernel's time, its algorithmic bytes and FLOPs and
+its fraction of the slower of its two bounds (HBM bytes at the measured copy
+peak, FLOPs at the measured bf16 tensor peak).
+
+With N > 1 each rank runs an independent replica on its own batch (different
+seed): no collective on the data path, weak scaling; a barrier and a
+max-over-ranks reduction bracket the timing.  Launched without torchrun,
+``--gpus N`` (N > 1) starts the N ranks itself through torch.distributed.run.
 
 The line printed by rank 0 also carries: the end-to-end figure through the
 host-buffer API (each step's pinned host inputs copied in and head outputs
 copied back, transfers overlapped across steps by HostDecodePipeline), the
-roofline of the attention kernel, the float64 oracle timed on a bounded sample
-on the host cores (cpu_baseline), GPU clocks sampled during the timed region,
-and the number of library kernels launched in the timed region.
+float64 oracle timed on a bounded sample on the host cores (cpu_baseline),
+GPU clocks sampled through NVML while the timed steps and an untimed soak of
+the same graph around them run, and the number of library kernels launched
+in the timed region.
 
 --impl reference times the float64 CPU oracle (the only reference this path
 has) on the same workload: each step is one sequence of the batch.
@@ -34,7 +47,6 @@ import re
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -49,6 +61,7 @@ DEFAULT_WORKLOAD = "sparse_b64_ctx16384_top2048"
 ROW_BYTES = (512 + 64) * 2          # one gathered cache row (latent + rotary), bf16
 FLUSH_BYTES = 256 << 20             # > 126 MB L2
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
 REF_HEADS = 64                     # heads per reference-arm step (a bounded sample of one query token)
 
 
@@ -88,82 +101,81 @@ def replica_seed(rank: int, base: int = 0) -> int:
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (100 ms) of the bench GPU; only samples taken
-    between mark_start() and mark_stop() (the timed region) are kept."""
+    """SM clock, its maximum, power and the clock-event reasons of the bench
+    GPU, read through NVML (queries only) every 20 ms by a background thread.
+    Only samples taken while a window is open (open_window / close_window)
+    are kept: the timed steps and the untimed soak of the same graph that
+    brackets them."""
 
-    FIELDS = ("timestamp,index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake_slowdown", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
-    def __init__(self, device_index: int):
-        self.proc = None
-        self.path = None
-        self.t0 = self.t1 = None
+    def __init__(self, device_index: int, period_s: float = 0.02):
+        import threading
+        self.period = period_s
+        self.samples = []
+        self.window = False
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.nvml = None
+        self.handle = None
         try:
+            import pynvml
+            pynvml.nvmlInit()
             props = torch.cuda.get_device_properties(device_index)
-            self.bus = f"{props.pci_bus_id:02X}:{props.pci_device_id:02X}."
-        except Exception:
-            self.bus = None
-
-    def start(self):
-        try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-f", self.path],
-                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
-            time.sleep(0.6)   # let the sampler come up before the timed region
-        except Exception:
-            self.proc = None
-
-    def mark_start(self):
-        self.t0 = time.time()
-
-    def mark_stop(self):
-        self.t1 = time.time()
-
-    def stop(self) -> dict | None:
-        if self.proc is None:
-            return None
-        time.sleep(0.15)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        import datetime
-        rows = []
-        try:
-            for line in open(self.path):
-                f = [x.strip() for x in line.split(",")]
-                if len(f) < 11:
-                    continue
-                try:
-                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                except ValueError:
-                    continue
-                if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
-                    continue
-                rows.append(f[1:])
-        finally:
-            os.unlink(self.path)
-        mine = [r for r in rows if self.bus and self.bus in r[1].upper()]
-        if mine or len({r[0] for r in rows}) > 1:
-            rows = mine
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-
-        def num(x):
+            bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
             try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
-        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                self.handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+            except Exception:
+                self.handle = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.nvml = pynvml
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def _run(self):
+        n = self.nvml
+        while not self.stop_flag.is_set():
+            if self.window:
+                try:
+                    sm = n.nvmlDeviceGetClockInfo(self.handle, n.NVML_CLOCK_SM)
+                    mx = n.nvmlDeviceGetMaxClockInfo(self.handle, n.NVML_CLOCK_SM)
+                    rs = n.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
+                    pw = n.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+                    self.samples.append((time.time(), sm, mx, rs, pw))
+                except Exception:
+                    pass
+            time.sleep(self.period)
+
+    def open_window(self):
+        self.window = True
+
+    def close_window(self):
+        self.window = False
+
+    def summary(self) -> dict:
+        self.stop_flag.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml"}
+        sm = [x[1] for x in self.samples]
+        mx = [x[2] for x in self.samples]
+        reasons = set()
+        for _, _, _, rs, _ in self.samples:
+            for name, const in self.REASONS:
+                bit = getattr(self.nvml, const, 0)
+                if bit and rs & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "power_w_max": max(x[4] for x in self.samples), "source": "nvml, every 20 ms",
+                "window": "the timed steps and an untimed soak of the same graph around them"}
 
 
 # ----------------------------------------------------------------- helpers
@@ -249,16 +261,31 @@ def oracle_sample(t: dict, wl, budget_s: float, max_seqs: int | None = None):
 
 
 # ----------------------------------------------------------------- our arm
+class L2Flush:
+    """Evicts L2 before a timed launch: writes a 256 MiB buffer (> the 126 MB
+    L2), then reads a second one, so that the lines left in L2 are clean and
+    none of the flush's dirty lines is written back during the timed work."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, i: int = 0):
+        self.w.fill_(i & 0xFF)
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
 def time_single_kernel(fn, n: int, flush) -> float:
     """Mean device time (ms) of fn(), which enqueues one library kernel on the
     current stream, with L2 flushed before each launch."""
     for i in range(3):
-        flush.fill_(i)
+        flush(i)
         fn()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
     torch.cuda.synchronize()
     for i in range(n):
-        flush.fill_((i + 5) & 0xFF)
+        flush((i + 5) & 0xFF)
         ev[2 * i].record()
         fn()
         ev[2 * i + 1].record()
@@ -342,7 +369,7 @@ def measure_multi_token(mla, step, d, B, K, rows, flush, n: int = 50) -> dict:
     torch.cuda.synchronize()
     with mla.ProfileHook() as hook:
         for i in range(n):
-            flush.fill_((i + 13) & 0xFF)
+            flush((i + 13) & 0xFF)
             hook.set_events(ev[2 * i], ev[2 * i + 1])
             call()
     torch.cuda.synchronize()
@@ -355,6 +382,113 @@ def measure_multi_token(mla, step, d, B, K, rows, flush, n: int = 50) -> dict:
             "kernel_ms": ms, "alg_bytes_per_launch": nbytes, "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
 
 
+FLOP_PER_ROW = 128 * (576 + 512) * 2   # scores (K=576) and PV (N=512) of all heads for one selected row
+
+
+def roofline(alg_bytes: int, flops: int, ms: float, hbm_gbs: float, tflops: float) -> dict:
+    """The slower of the kernel's two bounds (HBM bytes at the copy peak,
+    FLOPs at the bf16 tensor peak) and the fraction of it the kernel reaches."""
+    t_hbm = alg_bytes / (hbm_gbs * 1e9)
+    t_tc = flops / (tflops * 1e12)
+    sec = ms * 1e-3
+    if t_hbm >= t_tc:
+        return {"bound": "hbm", "achieved": alg_bytes / sec / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": t_hbm / sec, "ideal_ms": t_hbm * 1e3, "other_bound_ms": t_tc * 1e3}
+    return {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tflops, "unit": "TFLOP/s",
+            "frac": t_tc / sec, "ideal_ms": t_tc * 1e3, "other_bound_ms": t_hbm * 1e3}
+
+
+def measure_workload(mla, synth, name: str, dev, flush, args, rank: int, world: int, peaks: dict,
+                     clocks=None, soak_s: float = 0.0):
+    """One named workload: the step (graph replays, L2 flushed before each)
+    and the attention kernel alone (library events around it).  Returns the
+    record, the device tensors, the host tensors and the step object."""
+    wl = synth.workload(name, seed=replica_seed(rank, args.seed))
+    t = synth.make_inputs(wl, seed=replica_seed(rank, args.seed))
+    d = {k: v.to(dev) for k, v in t.items()}
+    B, K = wl.B, wl.row_stride()
+    rows = selected_rows(d["topk_idx"], d["end_pos"])
+    step = mla.DecodeStep(B, K, device=dev)
+    args_dev = (d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+    graph = mla.CapturedStep(step, *args_dev)
+    for i in range(args.warmup):
+        flush(i)
+        graph()
+    torch.cuda.synchronize()
+
+    # ---- the timed steps, each one replay of the captured step; an untimed
+    # soak of the same replays around them keeps the clocks sampled
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    if clocks is not None:
+        clocks.open_window()
+        t_end = time.perf_counter() + soak_s
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                graph()
+            torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush(i + 7)
+        st[2 * i].record()
+        graph()
+        st[2 * i + 1].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    barrier(world)
+    if clocks is not None:
+        t_end = time.perf_counter() + soak_s
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                graph()
+            torch.cuda.synchronize()
+        clocks.close_window()
+    step.check_status()
+    step_ms = [st[2 * i].elapsed_time(st[2 * i + 1]) for i in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world, dev)
+
+    # ---- the attention kernel alone: CUDA events recorded by the library on
+    # the launching stream right before and after it (these steps are not the
+    # timed ones: an event between two kernels separates them)
+    n_kern = max(3, min(args.steps, args.kernel_steps))
+    kt = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_kern)]
+    for ev in kt:       # the library re-records these on the launching stream; a first record
+        ev.record()     # through torch marks them recorded for torch's elapsed_time()
+    torch.cuda.synchronize()
+    with mla.ProfileHook() as khook:
+        for i in range(n_kern):
+            flush(i + 11)
+            khook.set_events(kt[2 * i], kt[2 * i + 1])
+            step(*args_dev)
+    torch.cuda.synchronize()
+    step.check_status()
+    kern_all = [kt[2 * i].elapsed_time(kt[2 * i + 1]) for i in range(n_kern)]
+    kern = statistics.mean(kern_all)
+
+    hbm = float(peaks.get("hbm_gbs") or FALLBACK_HBM_GBS)
+    tf = float(peaks.get("bf16_tflops") or FALLBACK_BF16_TFLOPS)
+    alg_bytes = rows * ROW_BYTES
+    flops = rows * FLOP_PER_ROW
+    step_bytes = alg_bytes + d["wkv_b"].numel() * 2
+    rec = {
+        "workload": name, "batch": B, "topk_row": K,
+        "end_pos": wl.end_pos[0] if len(set(wl.end_pos)) == 1 else f"{min(wl.end_pos)}..{max(wl.end_pos)}",
+        "selection": wl.selection, "selected_rows": rows,
+        "ms_per_step": ms_max, "ms_per_step_median": statistics.median(step_ms),
+        "tokens_per_s": world * B / (ms_max * 1e-3),
+        "kernel_ms": kern, "kernel_ms_median": statistics.median(kern_all),
+        "alg_bytes_per_launch": alg_bytes, "flops_per_launch": flops,
+        "roofline": roofline(alg_bytes, flops, kern, hbm, tf),
+        "step_roofline": {"bytes": step_bytes, "ideal_ms": step_bytes / (hbm * 1e9) * 1e3,
+                          "frac": step_bytes / (hbm * 1e9) * 1e3 / ms_max,
+                          "note": "gathered rows x 1152 B + one read of wkv_b, at the copy peak"},
+        "launches_per_step": graph.kernels_per_replay, "wall_s_timed_region": wall,
+    }
+    return rec, d, t, wl, step, graph
+
+
 def run_ours(args):
     from sparse_latent_attention_decode_b300 import mla, synth
 
@@ -364,64 +498,33 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
     dev = torch.device("cuda", local)
-
-    wl = synth.workload(args.workload, seed=replica_seed(rank, args.seed))
-    t = synth.make_inputs(wl, seed=replica_seed(rank, args.seed))
-    d = {k: v.to(dev) for k, v in t.items()}
-    B, K = wl.B, wl.row_stride()
-    rows = selected_rows(d["topk_idx"], d["end_pos"])
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    step = mla.DecodeStep(B, K, device=dev)
-    args_dev = (d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
-
-    # ---- device-resident inputs: the timed steps, each one replay of the step
-    # captured in a CUDA graph (kernels chained by programmatic dependent
-    # launch, nothing recorded between them)
-    graph = mla.CapturedStep(step, *args_dev)
-    for i in range(args.warmup):
-        flush.fill_(i & 0xFF)
-        graph()
-    torch.cuda.synchronize()
-    st = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    flush = L2Flush(dev)
+    peaks = measured_peaks()
+    peak_src = "measured" if peaks.get("hbm_gbs") else "fallback"
     clocks = ClockSampler(local)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.mark_start()
-    t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_((i + 7) & 0xFF)
-        st[2 * i].record()
-        graph()
-        st[2 * i + 1].record()
-    launches = graph.kernels_per_replay * args.steps
-    torch.cuda.synchronize()
-    barrier(world)
-    wall = time.perf_counter() - t_wall
-    clocks.mark_stop()
-    clk = clocks.stop()
-    step.check_status()
-    step_ms = [st[2 * i].elapsed_time(st[2 * i + 1]) for i in range(args.steps)]
-    ms = statistics.mean(step_ms)
-    ms_max = max_over_ranks(ms, world, dev)
-    ms_median = statistics.median(step_ms)
 
-    # ---- the attention kernel alone: CUDA events recorded by the library on
-    # the launching stream right before and after it (these steps are not the
-    # timed ones: an event between two kernels separates them)
-    n_kern = min(args.steps, args.kernel_steps)
-    kt = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_kern)]
-    for ev in kt:       # the library re-records these on the launching stream; a first record
-        ev.record()     # through torch marks them recorded for torch's elapsed_time()
-    torch.cuda.synchronize()
-    with mla.ProfileHook() as khook:
-        for i in range(n_kern):
-            flush.fill_((i + 11) & 0xFF)
-            khook.set_events(kt[2 * i], kt[2 * i + 1])
-            step(*args_dev)
-    torch.cuda.synchronize()
-    step.check_status()
-    kern = statistics.mean(kt[2 * i].elapsed_time(kt[2 * i + 1]) for i in range(n_kern))
+    names = [args.workload]
+    if args.configs == "all":
+        names += [n for n in synth.WORKLOADS if n != args.workload]
+    elif args.configs not in ("none", ""):
+        names += [n for n in args.configs.split(",") if n and n != args.workload]
+
+    configs = {}
+    head = None
+    for name in names:
+        is_head = name == args.workload
+        rec, d, t, wl, step, graph = measure_workload(mla, synth, name, dev, flush, args, rank, world, peaks,
+                                                      clocks=clocks if is_head else None,
+                                                      soak_s=args.clock_soak if is_head else 0.0)
+        configs[name] = rec
+        if is_head:
+            head = (rec, d, t, wl, step, graph)
+        else:
+            del d, t, step, graph
+            torch.cuda.empty_cache()
+    clk = clocks.summary()
+    rec, d, t, wl, step, graph = head
+    B, K = wl.B, wl.row_stride()
 
     # ---- end to end through the host-buffer API: every step copies its inputs
     # in from pinned host memory and its head outputs back; the pipeline
@@ -450,22 +553,21 @@ def run_ours(args):
 
     next_rows = measure_next_rows(mla, synth, dev, flush, args.seed, n=args.next_steps)
     if B % 2 == 0:
-        next_rows["multi_token_decode"] = measure_multi_token(mla, step, d, B, K, rows, flush, n=args.next_steps)
+        next_rows["multi_token_decode"] = measure_multi_token(mla, step, d, B, K, rec["selected_rows"], flush,
+                                                              n=args.next_steps)
 
     if rank != 0:
         return None
 
-    peaks = measured_peaks()
-    hbm = peaks.get("hbm_gbs")
-    peak_src = "measured" if hbm else "fallback"
-    hbm = float(hbm) if hbm else FALLBACK_HBM_GBS
-    alg_bytes = rows * ROW_BYTES
-    achieved = alg_bytes / (kern * 1e-3) / 1e9
+    hbm = float(peaks.get("hbm_gbs") or FALLBACK_HBM_GBS)
     read_peak = read_stream_gbs(dev)
-    # the whole step's ideal time: the gathered rows plus one read of wkv_b
-    step_bytes = alg_bytes + d["wkv_b"].numel() * 2
-    step_ideal_ms = step_bytes / (hbm * 1e9) * 1e3
     traffic = traffic_record()
+    roof = dict(rec["roofline"])
+    roof.update({"kernel": "mla_sparse_decode attention kernel", "traffic": traffic,
+                 "peak_source": f"{peak_src} hbm_gbs / bf16_tflops (burst: the kernel is timed alone)",
+                 "alg_bytes_per_launch": rec["alg_bytes_per_launch"], "flops_per_launch": rec["flops_per_launch"],
+                 "kernel_ms": rec["kernel_ms"], "read_stream_gbs": read_peak,
+                 "frac_of_read_stream": rec["alg_bytes_per_launch"] / (rec["kernel_ms"] * 1e-3) / 1e9 / read_peak})
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -475,33 +577,29 @@ def run_ours(args):
                          f"cycling over the {B} of the batch); float64 numpy, full step per sequence (RoPE, "
                          f"absorb, masked scores over all end_pos keys, softmax, PV, up-projection); {secs:.1f} s"}
 
+    ms_max = rec["ms_per_step"]
     line = {
         "metric": METRIC, "value": world * B / (ms_max * 1e-3), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "ms_per_step_median": ms_median,
-        "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "ms_per_step_median": rec["ms_per_step_median"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "batch_per_gpu": B, "global_batch": world * B,
-                   "end_pos": (wl.end_pos[0] if len(set(wl.end_pos)) == 1 else
-                               f"{min(wl.end_pos)}..{max(wl.end_pos)}"),
-                   "topk_row": K, "selected_rows_per_gpu": rows, "S_cap": wl.S_cap, "heads": 128,
-                   "kv_lora": 512, "rope_dim": 64, "l2": "flushed by a 256 MiB write before each step",
+                   "end_pos": rec["end_pos"], "topk_row": K, "selected_rows_per_gpu": rec["selected_rows"],
+                   "S_cap": wl.S_cap, "heads": 128, "kv_lora": 512, "rope_dim": 64,
+                   "l2": "flushed before each timed step (256 MiB written, then 256 MiB read)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": pipe.h2d_bytes(), "d2h_bytes_per_step": pipe.d2h_bytes(),
                 "path": "HostDecodePipeline: per-step copies in and out, overlapped across steps; no L2 flush "
                         "(the caches exceed L2)"},
-        "roofline": {"bound": "hbm", "kernel": "mla_sparse_decode attention kernel",
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
-                     "alg_bytes_per_launch": alg_bytes, "kernel_ms": kern,
-                     "read_stream_gbs": read_peak, "frac_of_read_stream": achieved / read_peak},
-        "step_roofline": {"bytes": step_bytes, "ideal_ms": step_ideal_ms, "frac": step_ideal_ms / ms_max,
-                          "note": "gathered rows x 1152 B + one read of wkv_b, at the copy peak"},
+        "roofline": roof,
+        "step_roofline": rec["step_roofline"],
+        "configs": {k: v for k, v in configs.items()},
         "cpu_baseline": cpu,
         "next_rows": {k: dict(v, frac=v["achieved_gbs"] / hbm) for k, v in next_rows.items()},
         "clocks": clk,
-        "gpu_launches": launches,
-        "wall_s_timed_region": wall,
+        "gpu_launches": rec["launches_per_step"] * args.steps,
+        "wall_s_timed_region": rec["wall_s_timed_region"],
     }
     return line
 
@@ -547,23 +645,43 @@ def run_reference(args):
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def spawn_ranks(argv, n: int) -> int:
+    """Start n ranks of this script through torch.distributed.run on this
+    node (rendezvous on 127.0.0.1); returns the launcher's exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000,
-                    help="timed steps (long enough for several clock samples)")
+    ap.add_argument("--steps", type=int, default=1000, help="timed steps per workload")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--kernel-steps", type=int, default=200,
                     help="extra steps in which the attention kernel alone is timed")
     ap.add_argument("--next-steps", type=int, default=50,
                     help="timed launches per added entry point (next_rows)")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, help="the headline workload")
+    ap.add_argument("--configs", default="all",
+                    help="workloads measured besides the headline: all, none, or a comma-separated list")
+    ap.add_argument("--clock-soak", type=float, default=1.0,
+                    help="seconds of untimed replays before and after the headline's timed steps, "
+                         "during which the clocks are sampled too")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # started without torchrun: one process per GPU, launched from here
+        raise SystemExit(spawn_ranks(argv, args.gpus))
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)

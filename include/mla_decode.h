@@ -75,6 +75,9 @@ typedef struct CUstream_st *mla_stream_t; /* same type as cudaStream_t */
 #define MLA_DEV_BAD_END_POS 1    /* end_pos[b] < 1 or > S_cap: sequence b skipped */
 #define MLA_DEV_BAD_POSITION 2   /* end_pos[b]-1 outside the rotary table */
 #define MLA_DEV_TIMEOUT 4        /* a bounded on-chip wait gave up */
+#define MLA_DEV_SCORE_RANGE 8    /* a partial score exceeded 2048 in magnitude: the
+                                    exchanged fp16 copy may be off by a whole unit
+                                    (see mla_sparse_decode, precision) */
 
 /* Rotary / YaRN parameters.  Defaults (mla_rope_params_default) are those of
  * the "Transformer blocks" page, excerpt model-args: max_seq_len 16384,
@@ -190,6 +193,15 @@ size_t mla_sparse_decode_workspace_size(int B, int K);
  *   workspace device scratch of at least mla_sparse_decode_workspace_size(B, K)
  *             bytes, 256-byte aligned; contents on entry do not matter.
  *   dev_status optional device int32, MLA_DEV_* bits OR-ed in.
+ * Precision: bf16 operands, fp32 accumulation, fp32 softmax.  The 576-wide
+ * score dot product is split in two halves computed on two SMs; each half's
+ * raw (unscaled) partial score reaches the other SM rounded to fp16, i.e. to
+ * 11 significant bits, so a score carries an extra error of at most
+ * 2^-12 * |partial|.  The seeded workloads reach |partial| of about 50 and
+ * the GPU tests check partials up to about 800 (logits softmax_scale *
+ * |partial| up to about 110) against the tolerance; a partial beyond 2048
+ * sets MLA_DEV_SCORE_RANGE, since the error of one exchanged copy can then
+ * reach a whole unit of the raw score.
  * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096,
  * K < 1 or > 1<<20, S_cap < 1), MLA_ERR_WORKSPACE. */
 int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla_bf16 *pe_cache,
@@ -307,6 +319,9 @@ int mla_weight_dequant_fp8(const uint8_t *w, const float *scale, int rows, int c
  *     B*128*512*2 bytes, so B <= 256).
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
+ *     The address is remembered with the context it belongs to: after a
+ *     cudaDeviceReset (a new primary context) the next call looks it up
+ *     again, so that call too should come before any capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing in it needs to start at zero.  Calls whose kernels
  *     overlap on the GPU (other streams, other host threads) race on it:

@@ -257,18 +257,6 @@ def attend_one(q_abs: np.ndarray, q_pe_rot: np.ndarray, kv: np.ndarray, pe: np.n
     return (o, p) if return_probs else o
 
 
-def sparse_attention(q_lat: np.ndarray, kv_cache: np.ndarray, pe_cache: np.ndarray,
-                     topk_idx: np.ndarray, end_pos: np.ndarray, scale: float,
-                     batches=None) -> np.ndarray:
-    """q_lat [B,H,576] = [q~ | rope(q_pe)]; returns o_lat [len(batches),H,512]."""
-    bs = range(q_lat.shape[0]) if batches is None else batches
-    out = []
-    for b in bs:
-        out.append(attend_one(q_lat[b, :, :KV_LORA], q_lat[b, :, KV_LORA:], kv_cache[b], pe_cache[b],
-                              topk_idx[b], int(end_pos[b]), scale))
-    return np.stack(out)
-
-
 # --------------------------------------------------------------------------
 # a8: value up-projection (mla-decode excerpt, last einsum)
 # --------------------------------------------------------------------------

@@ -93,6 +93,7 @@ constexpr int WG_THREADS = 128;
 constexpr int REG_GATHER = 72, REG_MMA = 56, REG_SOFTMAX = 136;
 static_assert(256 * REG_GATHER + 128 * REG_MMA + 256 * REG_SOFTMAX <= THREADS * 96, "register split");
 constexpr float RESCALE_T = 8.f;             // lazy-max threshold (log2 units)
+constexpr float SCORE_RANGE = 2048.f;        // largest partial score sent without MLA_DEV_SCORE_RANGE
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
 struct Params {
@@ -180,13 +181,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     if (!seq_ok && tid == 0 && r == 0 && split == 0) report(p.status, MLA_DEV_BAD_END_POS);
 
     // the unit's selection, padded to whole blocks; padding and positions
-    // outside [0, end_pos) become -1
+    // outside [0, end_pos) become -1 (four independent loads per thread)
     {
         const int32_t *sel = p.topk + (size_t)b * p.K;
-        for (int i = tid; i < nblk * NK; i += THREADS) {
-            const int slot = t0 + i;
-            const int id = slot < t1 ? sel[slot] : -1;
-            sidx[i] = (id >= 0 && id < e) ? id : -1;
+        const int n = nblk * NK;
+        for (int i0 = tid; i0 < n; i0 += 4 * THREADS) {
+            int id[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * THREADS, slot = t0 + i;
+                id[u] = (i < n && slot < t1) ? sel[slot] : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * THREADS;
+                if (i < n) sidx[i] = (id[u] >= 0 && id[u] < e) ? id[u] : -1;
+            }
         }
     }
     if (tid == 0) {
@@ -398,6 +408,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                     x[48 + q] = __uint_as_float(v3[q]);
                 }
             }
+            {
+                // the partial scores travel to the peer as fp16, rounded to 11 significant
+                // bits: flag magnitudes where that rounding reaches one unit of the raw score
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < 64; ++q) a[q & 3] = fmaxf(a[q & 3], fabsf(x[q]));
+                if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) > SCORE_RANGE) report(p.status, MLA_DEV_SCORE_RANGE);
+            }
             // ring credit: the peer's block j-1 has been received here (by the other
             // warpgroup), and PV(j-2) has read P(j-2) from its slot
             if (j >= 1 && !warp_wait(&bars.recv_full[(j - 1) % NRECV], ((j - 1) / NRECV) & 1, deadline)) {
@@ -536,34 +554,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             }
         }
         if (!ok) fail(p);
-        // warpgroup w normalises columns [128 w, 128 w + 128) of O_r
-        const bool have = ok && nblk > 0 && lt > 0.f;
+        // warpgroup w normalises columns [128 w, 128 w + 128) of O_r.  The rows
+        // leave TMEM one head per thread; they are staged in shared memory (the
+        // gather stages, idle once the last PV has completed) and then written
+        // out by whole rows, so that every global store is coalesced.
+        const bool tload = ok && nblk > 0;   // warp-uniform: tcgen05.ld is warp-collective
+        const bool have = tload && lt > 0.f;
         const float inv = have ? 1.f / lt : 0.f;
-        const size_t orow = p.n_split == 1 ? ((size_t)b * H + h) * C : ((size_t)unit * H + h) * C;
-        const int col0 = 256 * r + 128 * w;
+        const bool bf16_out = p.n_split == 1 && p.o_b16;
+        const int rowb = bf16_out ? 256 : 512;       // bytes of this warpgroup's part of one row
+        const uint32_t stg = smem_u32(stages) + w * (H * 512);
+        const uint32_t srow = stg + h * rowb;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-            float o[16];
-            if (have) {
-                uint32_t v[16];
-                tmem_ld16(trow + O_COL + 128 * w + c0, v);
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t v0[16], v1[16];
+            if (tload) {
+                tmem_ld16(trow + O_COL + 128 * w + c0, v0);
+                tmem_ld16(trow + O_COL + 128 * w + c0 + 16, v1);
                 tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 16; ++q) o[q] = __uint_as_float(v[q]) * inv;
-            } else {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) o[q] = 0.f;
             }
-            if (p.n_split == 1 && p.o_b16) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o_b16 + orow + col0 + c0);
-                dst[0] = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
-                                    pack_bf16(o[6], o[7]));
-                dst[1] = make_uint4(pack_bf16(o[8], o[9]), pack_bf16(o[10], o[11]), pack_bf16(o[12], o[13]),
-                                    pack_bf16(o[14], o[15]));
-            } else {
-                float4 *dst = reinterpret_cast<float4 *>((p.n_split == 1 ? p.o_out : p.part_o) + orow + col0 + c0);
+            float o[32];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            for (int q = 0; q < 16; ++q) {
+                o[q] = have ? __uint_as_float(v0[q]) * inv : 0.f;
+                o[16 + q] = have ? __uint_as_float(v1[q]) * inv : 0.f;
+            }
+            if (bf16_out) {
+                // 32 columns = 4 chunks of 16 bytes; chunk c of the row sits at c ^ (h & 7)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = c0 / 8 + i;
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(srow + ((c ^ (h & 7)) << 4)),
+                                 "r"(pack_bf16(o[8 * i], o[8 * i + 1])), "r"(pack_bf16(o[8 * i + 2], o[8 * i + 3])),
+                                 "r"(pack_bf16(o[8 * i + 4], o[8 * i + 5])), "r"(pack_bf16(o[8 * i + 6], o[8 * i + 7]))
+                                 : "memory");
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = c0 / 4 + i;
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(srow + ((c ^ (h & 7)) << 4)),
+                                 "f"(o[4 * i]), "f"(o[4 * i + 1]), "f"(o[4 * i + 2]), "f"(o[4 * i + 3])
+                                 : "memory");
+                }
+            }
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + w), "r"(WG_THREADS) : "memory");
+        {
+            const int col0 = 256 * r + 128 * w;
+            const int nch = rowb / 16;                 // 16-byte chunks per row part
+            const size_t row0 = bf16_out || p.n_split == 1 ? (size_t)b * H : (size_t)unit * H;
+            uint8_t *dst = bf16_out ? reinterpret_cast<uint8_t *>(p.o_b16 + row0 * C + col0)
+                                    : reinterpret_cast<uint8_t *>((p.n_split == 1 ? p.o_out : p.part_o) + row0 * C + col0);
+            const size_t pitch = bf16_out ? C * 2 : C * 4;   // bytes between the rows of two heads
+#pragma unroll 4
+            for (int idx = wtid; idx < H * nch; idx += WG_THREADS) {
+                const int row = idx / nch, c = idx % nch;
+                uint32_t a0, a1, a2, a3;
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                             : "r"(stg + row * rowb + ((c ^ (row & 7)) << 4)));
+                *reinterpret_cast<uint4 *>(dst + row * pitch + c * 16) = make_uint4(a0, a1, a2, a3);
             }
         }
         if (p.n_split > 1 && w == 0)

@@ -7,6 +7,9 @@
 #include "common.cuh"
 #include "kernels.cuh"
 
+#include <cstring>
+#include <mutex>
+
 namespace mla {
 
 struct WsLayout {
@@ -84,16 +87,23 @@ extern "C" const char *mla_status_string(int code) {
         case MLA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
         default: break;
     }
-    if (code > 0) {
-        static const char *names[8] = {"none",
-                                       "bad end_pos",
-                                       "position outside rotary table",
-                                       "bad end_pos; position outside rotary table",
-                                       "on-chip wait timed out",
-                                       "bad end_pos; on-chip wait timed out",
-                                       "position outside rotary table; on-chip wait timed out",
-                                       "bad end_pos; position outside rotary table; on-chip wait timed out"};
-        return names[code & 7];
+    if (code > 0 && code < 16) {
+        // one description per combination of the MLA_DEV_* bits
+        static const char *bit_names[4] = {"bad end_pos", "position outside rotary table",
+                                           "on-chip wait timed out", "partial score outside the exchange range"};
+        static char names[16][160];
+        static std::once_flag once;
+        std::call_once(once, [] {
+            for (int c = 1; c < 16; ++c) {
+                names[c][0] = 0;
+                for (int i = 0; i < 4; ++i) {
+                    if (!(c & (1 << i))) continue;
+                    if (names[c][0]) strcat(names[c], "; ");
+                    strcat(names[c], bit_names[i]);
+                }
+            }
+        });
+        return names[code];
     }
     return "unknown status code";
 }

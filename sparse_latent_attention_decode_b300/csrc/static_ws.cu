@@ -11,6 +11,8 @@
 #include "common.cuh"
 #include "kernels.cuh"
 
+#include <cuda.h>
+
 #include <mutex>
 
 namespace {
@@ -21,11 +23,30 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_ws[MLA_STATIC_WS_BYTES];
 
 // Device address of g_static_ws per device.  The name g_static_ws in host
-// code is only a host-side stand-in, so the address is looked up once per
-// device, with that device current.
+// code is only a host-side stand-in, so the address is looked up with that
+// device current.  The lookup is cached together with the context it was
+// made in: after cudaDeviceReset (or any re-creation of the primary context)
+// the library's device image is loaded again, possibly at another address,
+// and the next call looks the address up afresh.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q{};
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
 struct StaticWsAddr {
     std::mutex mu;
     void *ptr[64] = {};
+    CUcontext ctx[64] = {};
 };
 
 StaticWsAddr &addr_table() {
@@ -37,12 +58,19 @@ int static_ws_ptr(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
     if (dev < 0 || dev >= 64) return MLA_ERR_DEVICE;
+    CtxGetCurrentFn get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS) return MLA_ERR_CUDA;
     StaticWsAddr &t = addr_table();
     std::lock_guard<std::mutex> lock(t.mu);
-    if (!t.ptr[dev]) {
+    if (!ctx || !t.ptr[dev] || t.ctx[dev] != ctx) {
+        // the lookup also makes the device's primary context current when no
+        // context is yet; the context is named after it
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return MLA_ERR_CUDA;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return MLA_ERR_CUDA;
         t.ptr[dev] = p;
+        t.ctx[dev] = ctx;
     }
     *out = t.ptr[dev];
     return MLA_OK;

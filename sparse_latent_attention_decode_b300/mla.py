@@ -22,6 +22,7 @@ MLA_OK = 0
 MLA_DEV_BAD_END_POS = 1
 MLA_DEV_BAD_POSITION = 2
 MLA_DEV_TIMEOUT = 4
+MLA_DEV_SCORE_RANGE = 8
 
 
 class MLAError(RuntimeError):

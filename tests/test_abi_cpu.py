@@ -103,7 +103,16 @@ def test_status_strings():
         assert mla.status_string(code) not in ("ok", "unknown status code")
     assert "end_pos" in mla.status_string(1)
     assert "timed out" in mla.status_string(4)
+    assert "exchange range" in mla.status_string(8)
+    # every combination of device bits names each of its bits
+    for code in range(1, 16):
+        s = mla.status_string(code)
+        assert ("end_pos" in s) == bool(code & 1)
+        assert ("rotary table" in s) == bool(code & 2)
+        assert ("timed out" in s) == bool(code & 4)
+        assert ("exchange range" in s) == bool(code & 8)
     assert mla.status_string(-99) == "unknown status code"
+    assert mla.status_string(16) == "unknown status code"
 
 
 def test_python_wrappers_reject_cpu_tensors():

@@ -70,3 +70,23 @@ def test_single_process_helpers_need_no_process_group():
     assert bench.max_over_ranks(3.25, 1) == 3.25
     bench.barrier(1)
     assert bench.replica_seed(0) == 0 and bench.replica_seed(1, base=5) != 5
+
+
+def test_bench_spawns_its_own_ranks_for_gpus_n():
+    # `bench.py --gpus 2` started without torchrun launches two ranks itself;
+    # rank 0 alone prints one line, and that line counts both.  The reference
+    # arm runs on the host, so the spawn path is exercised without a GPU.
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    out = subprocess.run([sys.executable, os.path.join(os.path.dirname(bench.__file__), "bench.py"),
+                          "--gpus", "2", "--impl", "reference", "--workload", "p1000_b1", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["impl"] == "reference"

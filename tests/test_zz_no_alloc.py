@@ -2,12 +2,12 @@
 
 It serves callers that cannot allocate device memory: its scratch is a fixed
 array inside the library.  These tests call it through the C ABI and check
-that it returns what mla_sparse_decode (caller-supplied workspace) returns,
-on two calls in a row, so that what one call leaves in the shared array
-cannot leak into the next.  The file is named to be collected last."""
+that it returns, bit for bit, what mla_sparse_decode (caller-supplied
+workspace) returns, and that both agree with the float64 oracle, on two calls
+in a row, so that what one call leaves in the shared array cannot leak into
+the next.  The file is named to be collected last."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -16,11 +16,6 @@ from tests import parity_util as U
 
 if torch.cuda.is_available():
     from sparse_latent_attention_decode_b300 import mla
-
-
-def _inputs(B, ep, k, K, S, seed):
-    t = synth.make_inputs(synth.small_workload(B, ep, k=k, K=K, S_cap=S), seed=seed)
-    return {n: v.cuda() for n, v in t.items()}
 
 
 def _q_lat(d):
@@ -37,7 +32,9 @@ def test_static_workspace_matches_caller_workspace_on_two_calls(with_wkv_b):
     cases = [dict(B=3, ep=[700, 513, 260], k=256, K=300, S=704, seed=21),
              dict(B=1, ep=[1001], k=1001, K=1001, S=1024, seed=22)]
     for c in cases:
-        d = _inputs(c["B"], c["ep"], c["k"], c["K"], c["S"], c["seed"])
+        t = synth.make_inputs(synth.small_workload(c["B"], c["ep"], k=c["k"], K=c["K"], S_cap=c["S"]),
+                              seed=c["seed"])
+        d = {n: v.cuda() for n, v in t.items()}
         q_lat = _q_lat(d)
         w = d["wkv_b"] if with_wkv_b else None
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -47,9 +44,13 @@ def test_static_workspace_matches_caller_workspace_on_two_calls(with_wkv_b):
                                               scale, wkv_b=w, dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        g, r = got.cpu().double().numpy(), ref.cpu().double().numpy()
-        assert np.all(np.isfinite(g))
-        U.assert_attn_close(g, r, "static workspace vs caller workspace")
+        # the same kernels on the same inputs: bit-identical to the caller-workspace call
+        assert torch.equal(got, ref), "static workspace differs from caller workspace"
+        # and, independently, within the tolerance of the float64 oracle
+        x = U.oracle_inputs(t)
+        bs = list(range(c["B"]))
+        ora = U.oracle_out(x, bs) if with_wkv_b else U.oracle_o_lat(x, bs, q_lat=synth.to_f64(q_lat.cpu()))
+        U.assert_attn_close(got.cpu().numpy(), ora, "static workspace vs oracle")
 
 
 def test_static_workspace_rejects_sizes_beyond_its_capacity():
