@@ -27,8 +27,9 @@ max-over-ranks reduction bracket the timing.  Launched without torchrun,
 ``--gpus N`` (N > 1) starts the N ranks itself through torch.distributed.run.
 
 The line printed by rank 0 also carries: the end-to-end figure through the
-host-buffer API (each step's pinned host inputs copied in and head outputs
-copied back, transfers overlapped across steps by HostDecodePipeline), the
+host-buffer API (each step's pinned host inputs copied in and bf16 head
+outputs copied back, one CUDA-graph replay per step, transfers overlapped
+across steps by CapturedHostPipeline), the
 float64 oracle timed on a bounded sample on the host cores (cpu_baseline),
 GPU clocks sampled through NVML while the timed steps and an untimed soak of
 the same graph around them run, and the number of library kernels launched
@@ -100,6 +101,43 @@ def replica_seed(rank: int, base: int = 0) -> int:
 
 
 # ----------------------------------------------------------------- clocks
+class _Nvml:
+    """The few read-only NVML queries the clock record needs, called through
+    ctypes on the driver's libnvidia-ml (no Python binding required)."""
+
+    CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        rc = self.lib.nvmlInit_v2()
+        if rc != 0:
+            raise RuntimeError(f"nvmlInit_v2 returned {rc}")
+        self.reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle(self, bus_id: str, index: int):
+        h = self.c.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), self.c.byref(h)) == 0:
+            return h
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(self.c.c_uint(index), self.c.byref(h)) == 0:
+            return h
+        raise RuntimeError(f"no NVML handle for {bus_id} / index {index}")
+
+    def sample(self, h):
+        u = self.c.c_uint()
+        m = self.c.c_uint()
+        r = self.c.c_ulonglong()
+        p = self.c.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, self.c.byref(u)) != 0:
+            raise RuntimeError("nvmlDeviceGetClockInfo failed")
+        self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, self.c.byref(m))
+        self.reasons(h, self.c.byref(r))
+        self.lib.nvmlDeviceGetPowerUsage(h, self.c.byref(p))
+        return int(u.value), int(m.value), int(r.value), p.value / 1000.0
+
+
 class ClockSampler:
     """SM clock, its maximum, power and the clock-event reasons of the bench
     GPU, read through NVML (queries only) every 20 ms by a background thread.
@@ -107,49 +145,47 @@ class ClockSampler:
     are kept: the timed steps and the untimed soak of the same graph that
     brackets them."""
 
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
-               ("hw_power_brake_slowdown", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
+    # NVML clock-event reason bits
+    REASONS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+               ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
 
     def __init__(self, device_index: int, period_s: float = 0.02):
         import threading
         self.period = period_s
         self.samples = []
+        self.errors = []
         self.window = False
         self.stop_flag = threading.Event()
         self.thread = None
         self.nvml = None
         self.handle = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
+            self.nvml = _Nvml()
             props = torch.cuda.get_device_properties(device_index)
-            bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
-            try:
-                self.handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
-            except Exception:
-                self.handle = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.nvml = pynvml
-        except Exception:
+            bus = (f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:"
+                   f"{getattr(props, 'pci_device_id', 0):02X}.0")
+            idx = device_index
+            visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            ids = [v.strip() for v in visible.split(",") if v.strip()]
+            if ids and all(v.isdigit() for v in ids) and device_index < len(ids):
+                idx = int(ids[device_index])
+            self.handle = self.nvml.handle(bus, idx)
+        except Exception as e:
+            self.errors.append(f"nvml: {e}")
             self.nvml = None
         if self.nvml is not None:
             self.thread = threading.Thread(target=self._run, daemon=True)
             self.thread.start()
 
     def _run(self):
-        n = self.nvml
         while not self.stop_flag.is_set():
             if self.window:
                 try:
-                    sm = n.nvmlDeviceGetClockInfo(self.handle, n.NVML_CLOCK_SM)
-                    mx = n.nvmlDeviceGetMaxClockInfo(self.handle, n.NVML_CLOCK_SM)
-                    rs = n.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
-                    pw = n.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+                    sm, mx, rs, pw = self.nvml.sample(self.handle)
                     self.samples.append((time.time(), sm, mx, rs, pw))
-                except Exception:
-                    pass
+                except Exception as e:
+                    if len(self.errors) < 4:
+                        self.errors.append(f"sample: {e}")
             time.sleep(self.period)
 
     def open_window(self):
@@ -163,19 +199,17 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=2)
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml"}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml",
+                    "errors": self.errors}
         sm = [x[1] for x in self.samples]
         mx = [x[2] for x in self.samples]
-        reasons = set()
-        for _, _, _, rs, _ in self.samples:
-            for name, const in self.REASONS:
-                bit = getattr(self.nvml, const, 0)
-                if bit and rs & bit:
-                    reasons.add(name)
+        reasons = sorted({name for x in self.samples for name, bit in self.REASONS if x[3] & bit})
         return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(self.samples),
-                "power_w_max": max(x[4] for x in self.samples), "source": "nvml, every 20 ms",
-                "window": "the timed steps and an untimed soak of the same graph around them"}
+                "reasons": reasons, "samples": len(self.samples),
+                "power_w_max": max(x[4] for x in self.samples),
+                "seconds": self.samples[-1][0] - self.samples[0][0], "source": "nvml (libnvidia-ml), every 20 ms",
+                "window": "the timed steps and an untimed soak of the same graph around them",
+                **({"errors": self.errors} if self.errors else {})}
 
 
 # ----------------------------------------------------------------- helpers
@@ -527,23 +561,29 @@ def run_ours(args):
     B, K = wl.B, wl.row_stride()
 
     # ---- end to end through the host-buffer API: every step copies its inputs
-    # in from pinned host memory and its head outputs back; the pipeline
-    # overlaps step i's transfers with its neighbours' compute.  No L2 flush
-    # here: the caches the step gathers from (1.2 GB) are far larger than L2.
-    h = {k: t[k].pin_memory() for k in ("q_nope", "q_pe", "topk_idx", "end_pos")}
-    pipe = mla.HostDecodePipeline(B, K, device=dev)
-    h_outs = [torch.empty(B, 128, 128, dtype=torch.float32).pin_memory() for _ in range(2)]
-    hargs = (h["q_nope"], h["q_pe"], h["topk_idx"], h["end_pos"], d["kv_cache"], d["pe_cache"], d["wkv_b"])
+    # in from pinned host memory and its head outputs (bf16, the dtype the
+    # output projection takes) back; each step is one replay of a CUDA graph
+    # holding the copies and the three library calls, and two buffer sets on
+    # two streams alternate so that one step's transfers overlap the other's
+    # compute.  No L2 flush here: the caches the step gathers from (1.2 GB)
+    # are far larger than L2.
+    pipe = mla.CapturedHostPipeline(B, K, d["kv_cache"], d["pe_cache"], d["wkv_b"], device=dev)
+    for k in range(2):
+        for name in ("q_nope", "q_pe", "topk_idx", "end_pos"):
+            pipe.host_inputs(k)[name].copy_(t[name])
     for i in range(args.warmup):
-        pipe.submit(*hargs, h_outs[i % 2])
+        pipe.submit()
     pipe.finish()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    cur = torch.cuda.current_stream(dev)
     e0.record()
+    for st_ in pipe.streams:
+        st_.wait_stream(cur)
     for i in range(args.steps):
-        pipe.submit(*hargs, h_outs[i % 2])
+        pipe.submit()
     pipe.finish()
     e1.record()
     torch.cuda.synchronize()
@@ -590,8 +630,10 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": pipe.h2d_bytes(), "d2h_bytes_per_step": pipe.d2h_bytes(),
-                "path": "HostDecodePipeline: per-step copies in and out, overlapped across steps; no L2 flush "
-                        "(the caches exceed L2)"},
+                "out_dtype": "bf16",
+                "path": "CapturedHostPipeline: each step one graph replay (pinned host inputs copied in, three "
+                        "library calls, head outputs copied back); two buffer sets on two streams overlap one "
+                        "step's copies with the other's compute; no L2 flush (the caches exceed L2)"},
         "roofline": roof,
         "step_roofline": rec["step_roofline"],
         "configs": {k: v for k, v in configs.items()},

@@ -342,6 +342,16 @@ int mla_sparse_decode_static_ws(const mla_bf16 *q_lat, const mla_bf16 *kv_cache,
  * Pass NULL for all three to clear.  Returns MLA_OK. */
 int mla_profile_hook(void *ev_start, void *ev_stop, int64_t *launch_count);
 
+/* Limit, in nanoseconds, of every bounded on-chip wait of the kernels
+ * (default 2e9, i.e. 2 s; 0 is taken as 1).  The pages have no counterpart:
+ * it is the failure-detection knob of this library.  A kernel whose wait runs
+ * out sets MLA_DEV_TIMEOUT in *dev_status, then waits (for at most 1 s more)
+ * for the copies and MMAs it has already issued, releases its tensor memory
+ * and returns, so the context stays usable.  Process-wide; read when a kernel
+ * is launched (a CUDA graph keeps the value captured with it).  Meant for
+ * tests that drive a wait past its limit; returns the previous limit. */
+uint64_t mla_set_wait_limit_ns(uint64_t ns);
+
 /* Static description of a return code or of a set of MLA_DEV_* bits
  * (pass the negative return code, or the status word as a positive value). */
 const char *mla_status_string(int code);

@@ -30,10 +30,8 @@ constexpr int SMEM_BYTES = 2 * A_BOX + 2 * B_BOX + 1024;
 // an SM, so the 512 CTAs run as one wave.
 __host__ __device__ constexpr int smem_bytes(int nmax) { return 2 * A_BOX + 2 * nmax * 128 + 1024; }
 constexpr int PAIRS_PER_TILE = NPAIR / 4;      // rotary pairs handled by each latent tile
-constexpr uint64_t TIMEOUT_NS = 2000000000ull;
-
 struct Bars {
-    uint64_t a_full, b_full, mma_done;
+    uint64_t a_full, b_full, mma_done, drain;
     uint32_t tmem_base;
 };
 
@@ -81,7 +79,7 @@ __global__ void __launch_bounds__(128)
     absorb_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
                   const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis, int max_seq_len,
                   const int32_t *__restrict__ end_pos, int B, int T, int nmax, uint16_t *__restrict__ q_lat,
-                  int32_t *status) {
+                  int32_t *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -92,6 +90,7 @@ __global__ void __launch_bounds__(128)
         mbar_init(&bars.a_full, 1);
         mbar_init(&bars.b_full, 1);
         mbar_init(&bars.mma_done, 1);
+        mbar_init(&bars.drain, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -104,8 +103,9 @@ __global__ void __launch_bounds__(128)
     // the attention grid may be scheduled as soon as every CTA of this one has started
     if (tid == 0) grid_dep_launch();
     const uint32_t tmem = bars.tmem_base;
-    const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
+    const Deadline deadline = make_deadline(wait_ns);
     bool ok = true;
+    int b_issued = 0;   // batch tiles whose loads tid 0 has issued
 
     if (tid == 0) {
         // W_UK[h] = rows h*256 .. h*256+127 of wkv_b; this tile = latent columns 128t .. 128t+127
@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(128)
             mbar_expect_tx(&bars.b_full, 2 * bbox);
             tma_load_3d(smem_u32(sB), &qmap, 0, h, n0, &bars.b_full);
             tma_load_3d(smem_u32(sB + bbox), &qmap, 64, h, n0, &bars.b_full);
+            b_issued = pass + 1;
         }
         if (pass == 0) rope_part(q_pe, cis, max_seq_len, end_pos, B, T, h, t, q_lat, status, tid);
         if (tid == 0) {
@@ -163,6 +164,16 @@ __global__ void __launch_bounds__(128)
         __syncthreads();   // TMEM and the batch tile are reused by the next pass
     }
     if (!ok && tid == 0) report(status, MLA_DEV_TIMEOUT);
+    if (tid == 0) {
+        // drain: the weight tile and the last batch tile have landed and every
+        // issued MMA has completed before the CTA releases TMEM and exits
+        const uint64_t drain = globaltimer_ns() + DRAIN_NS;
+        bool landed = wait_until(&bars.a_full, 0, drain);
+        if (b_issued > 0) landed = wait_until(&bars.b_full, (b_issued - 1) & 1, drain) && landed;
+        mma_commit(&bars.drain);
+        landed = wait_until(&bars.drain, 0, drain) && landed;
+        if (!landed) report(status, MLA_DEV_TIMEOUT);
+    }
 
     tc_fence_before();
     __syncthreads();
@@ -210,7 +221,8 @@ extern "C" int mla_absorb_q_tokens(const mla_bf16 *q_nope, const mla_bf16 *q_pe,
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     absorb::absorb_kernel<<<dim3(4, H), 128, absorb::smem_bytes(nmax), s>>>(
-        wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, T, nmax, q_lat, dev_status);
+        wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, T, nmax, q_lat, dev_status,
+        wait_limit_ns());
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

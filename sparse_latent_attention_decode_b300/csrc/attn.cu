@@ -94,7 +94,6 @@ constexpr int REG_GATHER = 72, REG_MMA = 56, REG_SOFTMAX = 136;
 static_assert(256 * REG_GATHER + 128 * REG_MMA + 256 * REG_SOFTMAX <= THREADS * 96, "register split");
 constexpr float RESCALE_T = 8.f;             // lazy-max threshold (log2 units)
 constexpr float SCORE_RANGE = 2048.f;        // largest partial score sent without MLA_DEV_SCORE_RANGE
-constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
 struct Params {
     const uint16_t *q_lat;
@@ -111,6 +110,7 @@ struct Params {
     float *part_o;      // n_split > 1: per-split normalised o, fp32 [B*n_split][128][512]
     float *part_lse;    // n_split > 1: log2 of the split's softmax mass, [B*n_split][2][128]
     int32_t *status;
+    uint64_t wait_ns;   // limit of every bounded wait
 };
 
 struct Bars {
@@ -120,6 +120,7 @@ struct Bars {
     uint64_t m_ready[2];   // m after block j is in mval[j % 2]
     uint64_t l_ready;      // both running sums are in lsum (the send buffer, after the last copy)
     uint64_t send_ready;   // the send buffer holds block j's partial scores
+    uint64_t drain[2];     // MMA issuers (QK, PV): every MMA they issued has completed
     int send_done;         // copies 0 .. send_done-1 have read the send buffer (a counter, not a
                            // barrier: the warpgroup of block j waits for the copy of block j-1
                            // without having seen the copy of block j-2 complete)
@@ -131,11 +132,11 @@ __device__ __forceinline__ void fail(const Params &p) { report(p.status, MLA_DEV
 
 // Bounded wait until a shared-memory counter written by another thread of the
 // CTA reaches `target` (warp-uniform result).
-__device__ __forceinline__ bool wait_count(const int *counter, int target, uint64_t deadline) {
+__device__ __forceinline__ bool wait_count(const int *counter, int target, const Deadline &deadline) {
     bool ok = true;
     for (uint32_t i = 0; *reinterpret_cast<const volatile int *>(counter) < target; ++i) {
         if (i >= 2) __nanosleep(32);
-        if ((i & 31) == 31 && globaltimer_ns() > deadline) {
+        if ((i & 31) == 31 && globaltimer_ns() > deadline.t) {
             ok = false;
             break;
         }
@@ -145,7 +146,7 @@ __device__ __forceinline__ bool wait_count(const int *counter, int target, uint6
 }
 
 // warp-uniform bounded waits: every lane of the warp takes the same branch afterwards
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t deadline) {
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Deadline &deadline) {
     return __all_sync(0xffffffffu, wait_until(bar, parity, deadline));
 }
 
@@ -211,6 +212,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         mbar_init(&bars.q_ready, 2 * WG_THREADS);
         mbar_init(&bars.l_ready, 2 * WG_THREADS);
         mbar_init(&bars.send_ready, WG_THREADS);
+        mbar_init(&bars.drain[0], 1);
+        mbar_init(&bars.drain[1], 1);
         bars.send_done = 0;
         for (int k = 0; k < NRECV; ++k) mbar_init(&bars.recv_full[k], 1);
         fence_mbar_init();
@@ -227,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     // returns once this grid -- and so the grid before it -- has completed.
     if (tid == 0) grid_dep_launch();
     const uint32_t tmem = bars.tmem_base;
-    const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
+    const Deadline deadline = make_deadline(p.wait_ns);
 
     if (warp < 8) {
         // ------------------------------------------------------------ gather producers
@@ -324,6 +327,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 }
             }
             if (!ok) fail(p);
+            // drain: every MMA this thread issued has completed before TMEM is released
+            mma_commit(&bars.drain[warp - QK_WARP]);
+            if (!wait_until(&bars.drain[warp - QK_WARP], 0, globaltimer_ns() + DRAIN_NS)) fail(p);
         }
         if (lane == 0 && nblk > 0 && warp == COPY_WARP) {
             // ships each block's partial scores to the peer's receive slot
@@ -340,6 +346,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 bulk_wait_read();
                 *reinterpret_cast<volatile int *>(&bars.send_done) = j + 1;
             }
+            // drain: every copy into the peer has been written before this CTA
+            // reaches the final cluster barrier (after which the peer may exit)
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroups (ping-pong)
@@ -636,8 +645,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
 __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_lse, int n_split,
                                                       float *__restrict__ o_out, uint16_t *__restrict__ o_b16) {
-    grid_dep_wait();   // the partials come from the preceding attention grid
+    // the dependent grid (the up-projection) may start loading its weights now;
+    // it reads this grid's output only after its own griddepcontrol.wait
     grid_dep_launch();
+    grid_dep_wait();   // the partials come from the preceding attention grid
     const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x * 4, half = c >= 256 ? 1 : 0;
     float M = -INFINITY;
     for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_lse[(((size_t)b * n_split + s) * 2 + half) * H + h]);
@@ -708,6 +719,7 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
     p.n_split = n_split;
     p.split_len = split_len;
     p.status = status;
+    p.wait_ns = wait_limit_ns();
     if (n_split == 1) {
         p.o_out = o_out;
         p.o_b16 = o_b16;

@@ -41,4 +41,13 @@ inline void count_launches(int n) {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Limit of the bounded on-chip waits of the kernels that drain their own
+// in-flight copies and MMAs before they give up (see mla_set_wait_limit_ns);
+// read at launch and passed to the kernel.
+uint64_t wait_limit_ns();
+// Every kernel that gives up a wait first waits, for at most this long, for
+// the copies and MMAs it has already issued, so that nothing it started
+// still writes its shared memory or tensor memory after it has released them.
+constexpr uint64_t DRAIN_NS = 1000000000ull;
+
 }  // namespace mla

@@ -7,6 +7,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -28,7 +29,16 @@ static WsLayout ws_layout(int B, int K) {
 
 }  // namespace mla
 
+namespace mla {
+static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+}  // namespace mla
+
 using namespace mla;
+
+extern "C" uint64_t mla_set_wait_limit_ns(uint64_t ns) {
+    return g_wait_limit_ns.exchange(ns == 0 ? 1ull : ns);
+}
 
 extern "C" size_t mla_sparse_decode_workspace_size(int B, int K) {
     if (B < 1 || B > 4096 || K < 1 || K > (1 << 20)) return 0;

@@ -32,10 +32,8 @@ constexpr int BK = 64;           // K per stage: one 128-byte swizzle row
 constexpr int NT_MAX = 256;      // token columns per CTA (MMA N)
 constexpr int STAGES = 4;
 constexpr int W_TILE = BN * BK * 2;   // 16 KB
-constexpr uint64_t TIMEOUT_NS = 2000000000ull;
-
 struct Bars {
-    uint64_t full[STAGES], empty[STAGES], acc_full;
+    uint64_t full[STAGES], empty[STAGES], acc_full, drain;
     uint32_t tmem_base;
 };
 
@@ -51,7 +49,7 @@ __global__ void __launch_bounds__(128) linear_kernel(const __grid_constant__ CUt
                                                      const __grid_constant__ CUtensorMap xmap, int M, int N, int K,
                                                      int NT, int kb_per_split, float *__restrict__ part,
                                                      float *__restrict__ y32, uint16_t *__restrict__ y16,
-                                                     int32_t *status) {
+                                                     int32_t *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -66,6 +64,7 @@ __global__ void __launch_bounds__(128) linear_kernel(const __grid_constant__ CUt
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars.full[s], 1), mbar_init(&bars.empty[s], 1);
         mbar_init(&bars.acc_full, 1);
+        mbar_init(&bars.drain, 1);
         fence_mbar_init();
     }
     if (warp == 2) {
@@ -76,12 +75,13 @@ __global__ void __launch_bounds__(128) linear_kernel(const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
+    const Deadline deadline = make_deadline(wait_ns);
     // X may be the output of the preceding grid of the stream
     grid_dep_wait();
 
     if (tid == 0) {
         // ---------------------------------------------------------------- TMA producer
+        int issued = 0;
         for (int i = 0; i < nkb; ++i) {
             const int s = i % STAGES;
             if (i >= STAGES && !wait_until(&bars.empty[s], ((i / STAGES) - 1) & 1, deadline)) {
@@ -92,7 +92,16 @@ __global__ void __launch_bounds__(128) linear_kernel(const __grid_constant__ CUt
             mbar_expect_tx(&bars.full[s], SB);
             tma_load_2d(smem_u32(st), &wmap, (kb0 + i) * BK, n0, &bars.full[s]);
             tma_load_2d(smem_u32(st + W_TILE), &xmap, (kb0 + i) * BK, m0, &bars.full[s]);
+            issued = i + 1;
         }
+        // drain: the loads of the last STAGES issued slices have landed (the
+        // earlier ones were consumed before their stage was reissued)
+        const uint64_t drain = globaltimer_ns() + DRAIN_NS;
+        for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+            if (!wait_until(&bars.full[i % STAGES], (i / STAGES) & 1, drain)) {
+                report(status, MLA_DEV_TIMEOUT);
+                break;
+            }
     } else if (tid == 32) {
         // ---------------------------------------------------------------- MMA issuer
         const uint32_t idesc = idesc_bf16(BN, NT, false, false);
@@ -113,13 +122,16 @@ __global__ void __launch_bounds__(128) linear_kernel(const __grid_constant__ CUt
             mma_commit(&bars.empty[s]);
         }
         if (ok) mma_commit(&bars.acc_full);
+        // drain: every MMA issued above has completed before TMEM can be released
+        mma_commit(&bars.drain);
+        if (!wait_until(&bars.drain, 0, globaltimer_ns() + DRAIN_NS)) report(status, MLA_DEV_TIMEOUT);
     }
     __syncwarp();
 
     // -------------------------------------------------------------------- epilogue
     // lane = weight row n0 + 32*warp + lane, column j = token m0 + j
     const bool ready = __all_sync(0xffffffffu, wait_until(&bars.acc_full, 0, deadline));
-    if (tid == 0 && !ready) report(status, MLA_DEV_TIMEOUT);
+    if (lane == 0 && !ready) report(status, MLA_DEV_TIMEOUT);   // this warp's rows are not written
     if (ready) {
         tc_fence_after();
         // let the next grid of the stream (the split reduction) start its prologue
@@ -247,7 +259,7 @@ extern "C" int mla_linear_bf16(const mla_bf16 *x, const mla_bf16 *w, int M, int 
     const dim3 grid((N + lin::BN - 1) / lin::BN, n_split, (M + NT - 1) / NT);
     float *part = n_split > 1 ? static_cast<float *>(workspace) : nullptr;
     if (launch_k(true, lin::linear_kernel, grid, dim3(128), smem, s, wmap, xmap, M, N, K, NT, kb_per, part, y_f32,
-                 reinterpret_cast<uint16_t *>(y_bf16), dev_status) != cudaSuccess)
+                 reinterpret_cast<uint16_t *>(y_bf16), dev_status, wait_limit_ns()) != cudaSuccess)
         return MLA_ERR_CUDA;
     int launches = 1;
     if (n_split > 1) {

@@ -28,10 +28,8 @@ constexpr int NMAX = 64;                       // sequences per pass
 constexpr int A_BOX = 128 * 128;               // [128 d][64 c] box of W_UV, bytes
 constexpr int B_ATOM = NMAX * 128;             // [64 b][64 c] atom column of the o tile, bytes
 constexpr int SMEM_BYTES = 8 * A_BOX + 8 * B_ATOM + 1024;
-constexpr uint64_t TIMEOUT_NS = 2000000000ull;
-
 struct Bars {
-    uint64_t a_full, b_full, mma_done;
+    uint64_t a_full, b_full, mma_done, drain;
     uint32_t tmem_base;
 };
 
@@ -70,7 +68,7 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
                                                         const __grid_constant__ CUtensorMap omap,
                                                         const float *__restrict__ o_f32, bool o_is_b16, int B,
                                                         float *__restrict__ out, uint16_t *__restrict__ out_b16,
-                                                        int32_t *status) {
+                                                        int32_t *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -81,6 +79,7 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
         mbar_init(&bars.a_full, 1);
         mbar_init(&bars.b_full, 1);
         mbar_init(&bars.mma_done, 1);
+        mbar_init(&bars.drain, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -91,7 +90,8 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
-    const uint64_t deadline = globaltimer_ns() + TIMEOUT_NS;
+    const Deadline deadline = make_deadline(wait_ns);
+    int b_issued = 0;   // o tiles whose loads tid 0 has issued
 
     if (tid == 0) {   // W_UV[h] = rows h*256+128 .. h*256+255 of wkv_b, 8 boxes of 64 latent columns
         mbar_expect_tx(&bars.a_full, 8 * A_BOX);
@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
             if (tid == 0) {   // 8 boxes [64 b][64 c] of o_h; rows beyond B are zero-filled
                 mbar_expect_tx(&bars.b_full, 8 * B_ATOM);
                 for (int a = 0; a < 8; ++a) tma_load_3d(smem_u32(sB + a * B_ATOM), &omap, 64 * a, h, n0, &bars.b_full);
+                b_issued = pass + 1;
             }
         } else {
             stage_f32(o_f32, h, n0, nb, N, sB, tid);
@@ -157,6 +158,16 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
         __syncthreads();   // TMEM and the operand tile are reused by the next pass
     }
     if (!ok && tid == 0) report(status, MLA_DEV_TIMEOUT);
+    if (tid == 0) {
+        // drain: W_UV and the last o tile have landed and every issued MMA has
+        // completed before the CTA releases TMEM and exits
+        const uint64_t drain = globaltimer_ns() + DRAIN_NS;
+        bool landed = wait_until(&bars.a_full, 0, drain);
+        if (b_issued > 0) landed = wait_until(&bars.b_full, (b_issued - 1) & 1, drain) && landed;
+        mma_commit(&bars.drain);
+        landed = wait_until(&bars.drain, 0, drain) && landed;
+        if (!landed) report(status, MLA_DEV_TIMEOUT);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -194,7 +205,7 @@ int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     const cudaError_t err = launch_k(pdl, outup::out_up_kernel, dim3(H), dim3(128), outup::SMEM_BYTES, s, wmap,
-                                     omap, o_f32, o_b16 != nullptr, B, out, out_b16, status);
+                                     omap, o_f32, o_b16 != nullptr, B, out, out_b16, status, wait_limit_ns());
     count_launches(1);
     return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

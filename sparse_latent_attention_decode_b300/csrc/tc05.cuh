@@ -53,6 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait with an explicit suspend-time hint (0: return at once)
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -231,6 +241,28 @@ __device__ __forceinline__ bool wait_until(uint64_t *bar, uint32_t parity, uint6
         if (mbar_try_wait(bar, parity)) return true;
         if (i >= 2) __nanosleep(i < 8 ? 32 : 96);
         if ((i & 31) == 31 && globaltimer_ns() > deadline) return false;
+    }
+}
+// A wait limit as seen by one thread: the global-timer deadline, and the
+// suspend hint of each poll.  Limits far above the default hint keep it; a
+// short limit (a test driving a wait past it) polls without suspending
+// (test_wait), so that the deadline is checked within a few microseconds.
+struct Deadline {
+    uint64_t t;
+    uint32_t hint;
+};
+__device__ __forceinline__ Deadline make_deadline(uint64_t limit_ns) {
+    const uint64_t h = limit_ns / 64;
+    return Deadline{globaltimer_ns() + limit_ns, h >= MBAR_SUSPEND_NS ? MBAR_SUSPEND_NS : uint32_t(h)};
+}
+__device__ __forceinline__ bool wait_until(uint64_t *bar, uint32_t parity, const Deadline &d) {
+#pragma unroll 1
+    for (uint32_t i = 0;; ++i) {
+        // a zero hint polls with the non-blocking test_wait and checks the
+        // deadline on every poll
+        if (d.hint ? mbar_try_wait_hint(bar, parity, d.hint) : mbar_test(bar, parity)) return true;
+        if ((d.hint == 0 || (i & 31) == 31) && globaltimer_ns() > d.t) return false;
+        if (i >= 2) __nanosleep(i < 8 ? 32 : 96);
     }
 }
 __device__ __forceinline__ bool wait_until_cluster(uint64_t *bar, uint32_t parity, uint64_t deadline) {

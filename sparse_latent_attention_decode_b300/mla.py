@@ -62,6 +62,7 @@ def _load():
         "mla_sparse_decode_tokens": (I, [P, P, P, I, P, I, P, I, I, F, P, P, I, P, Z, P, P]),
         "mla_linear_workspace_size": (Z, [I, I, I]),
         "mla_linear_bf16": (I, [P, P, I, I, I, P, P, P, Z, P, P]),
+        "mla_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -76,8 +77,14 @@ EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
             "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws", "mla_weight_dequant_fp8",
             "mla_cache_append", "mla_absorb_q_tokens", "mla_sparse_decode_tokens",
-            "mla_linear_workspace_size", "mla_linear_bf16")
+            "mla_linear_workspace_size", "mla_linear_bf16", "mla_set_wait_limit_ns")
 STATIC_WS_BYTES = 32 << 20
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of the kernels' bounded on-chip waits (process-wide); returns the
+    previous limit.  See mla_set_wait_limit_ns in include/mla_decode.h."""
+    return int(_lib.mla_set_wait_limit_ns(int(ns)))
 
 
 def status_string(code: int) -> str:
@@ -424,20 +431,28 @@ class DecodeStep:
     stream.  The caches and wkv_b are resident device state; the per-step
     inputs are the query parts, the selection and end_pos."""
 
-    def __init__(self, B: int, K: int, device="cuda", params: RopeParams | None = None):
+    def __init__(self, B: int, K: int, device="cuda", params: RopeParams | None = None,
+                 out_dtype=torch.float32):
+        if out_dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
         self.B, self.K, self.device = B, K, torch.device(device)
         self.params = params if params is not None else rope_params()
         self.scale = softmax_scale(self.params)
         self.cis = rope_freqs_init(self.params, device=self.device)
         self.q_lat = torch.empty(B, N_HEADS, Q_LAT, dtype=torch.bfloat16, device=self.device)
-        self.out = torch.empty(B, N_HEADS, D_V, dtype=torch.float32, device=self.device)
+        self.out = torch.empty(B, N_HEADS, D_V, dtype=out_dtype, device=self.device)
         self.workspace = torch.empty(workspace_size(B, K), dtype=torch.uint8, device=self.device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
 
     def __call__(self, q_nope, q_pe, kv_cache, pe_cache, wkv_b, topk_idx, end_pos):
         mla_absorb_q(q_nope, q_pe, self.cis, end_pos, wkv_b, out=self.q_lat, dev_status=self.status)
-        return mla_sparse_decode(self.q_lat, kv_cache, pe_cache, topk_idx, end_pos, self.scale, wkv_b=wkv_b,
-                                 out=self.out, workspace=self.workspace, dev_status=self.status)
+        if self.out.dtype == torch.float32:
+            return mla_sparse_decode(self.q_lat, kv_cache, pe_cache, topk_idx, end_pos, self.scale, wkv_b=wkv_b,
+                                     out=self.out, workspace=self.workspace, dev_status=self.status)
+        out = mla_sparse_decode_tokens(self.q_lat[:, None], kv_cache, pe_cache, topk_idx[:, None], end_pos,
+                                       self.scale, wkv_b=wkv_b, out=self.out[:, None], workspace=self.workspace,
+                                       dev_status=self.status, out_dtype=torch.bfloat16)
+        return out[:, 0]
 
     def check_status(self):
         v = int(self.status.item())
@@ -450,14 +465,15 @@ class HostDecodeStep(DecodeStep):
     pinned host memory to the device, the three library calls run, and the
     head outputs are copied back into a pinned host buffer."""
 
-    def __init__(self, B: int, K: int, device="cuda", params: RopeParams | None = None):
-        super().__init__(B, K, device, params)
+    def __init__(self, B: int, K: int, device="cuda", params: RopeParams | None = None,
+                 out_dtype=torch.float32):
+        super().__init__(B, K, device, params, out_dtype)
         dev = self.device
         self.d_q_nope = torch.empty(B, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=dev)
         self.d_q_pe = torch.empty(B, N_HEADS, D_ROPE, dtype=torch.bfloat16, device=dev)
         self.d_topk = torch.empty(B, K, dtype=torch.int32, device=dev)
         self.d_end = torch.empty(B, dtype=torch.int32, device=dev)
-        self.h_out = torch.empty(B, N_HEADS, D_V, dtype=torch.float32).pin_memory()
+        self.h_out = torch.empty(B, N_HEADS, D_V, dtype=out_dtype).pin_memory()
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in (self.d_q_nope, self.d_q_pe, self.d_topk, self.d_end))
@@ -528,6 +544,66 @@ class HostDecodePipeline:
         compute = torch.cuda.current_stream(self.device)
         for k in range(min(self.count, 2)):
             compute.wait_event(self.copied_out[k])
+
+    def check_status(self):
+        for st in self.steps:
+            st.check_status()
+
+
+class CapturedHostPipeline:
+    """End-to-end decode steps from pinned host buffers, each step one CUDA
+    graph replay: the graph copies the step's query parts, selection and
+    end_pos in from pinned host memory, runs absorption, attention and
+    up-projection, and copies the head outputs back into pinned host memory.
+    Two buffer sets, each with its own graph and stream, alternate, so that
+    one step's transfers overlap the other's compute, and the host makes one
+    call per step (a slow host does not pace the device).
+
+    Fill ``host_inputs(i)`` before ``submit(i)``; read ``host_output(i)``
+    after ``finish()``.  Step i uses buffer set i % 2: do not refill it
+    before the step two submissions earlier has finished (``finish``)."""
+
+    def __init__(self, B: int, K: int, kv_cache, pe_cache, wkv_b, device="cuda",
+                 params: RopeParams | None = None, out_dtype=torch.bfloat16):
+        self.device = torch.device(device)
+        self.steps, self.h_in, self.graphs, self.streams = [], [], [], []
+        for _ in range(2):
+            st = HostDecodeStep(B, K, self.device, params, out_dtype)
+            h = {"q_nope": torch.zeros(B, N_HEADS, D_NOPE, dtype=torch.bfloat16).pin_memory(),
+                 "q_pe": torch.zeros(B, N_HEADS, D_ROPE, dtype=torch.bfloat16).pin_memory(),
+                 "topk_idx": torch.full((B, K), -1, dtype=torch.int32).pin_memory(),
+                 "end_pos": torch.ones(B, dtype=torch.int32).pin_memory()}
+            g = CapturedStep(st.run, h["q_nope"], h["q_pe"], h["topk_idx"], h["end_pos"], kv_cache, pe_cache,
+                             wkv_b)
+            self.steps.append(st)
+            self.h_in.append(h)
+            self.graphs.append(g)
+            self.streams.append(torch.cuda.Stream(self.device))
+        self.count = 0
+
+    def host_inputs(self, i: int) -> dict:
+        return self.h_in[i % 2]
+
+    def host_output(self, i: int) -> torch.Tensor:
+        return self.steps[i % 2].h_out
+
+    def h2d_bytes(self):
+        return self.steps[0].h2d_bytes()
+
+    def d2h_bytes(self):
+        return self.steps[0].d2h_bytes()
+
+    def submit(self):
+        k = self.count % 2
+        with torch.cuda.stream(self.streams[k]):
+            self.graphs[k]()
+        self.count += 1
+
+    def finish(self):
+        """Make the current stream wait for every submitted step."""
+        cur = torch.cuda.current_stream(self.device)
+        for s in self.streams:
+            cur.wait_stream(s)
 
     def check_status(self):
         for st in self.steps:

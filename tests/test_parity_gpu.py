@@ -690,3 +690,30 @@ def test_maximum_batch_of_query_rows():
     U.assert_attn_close(got[bs], U.oracle_out(x, bs), "B=4096 sampled sequences")
     with pytest.raises(mla.MLAError):
         mla.DecodeStep(B + 1, K)                # one row past the limit: no workspace size
+
+
+def test_captured_host_pipeline_steps_match_their_inputs():
+    # the end-to-end path bench.py times: each step one graph replay that copies
+    # the step's pinned host inputs in and its bf16 head outputs back
+    B, K, n = 3, 256, 5
+    t = synth.make_inputs(synth.small_workload(B, [700, 256, 1000], k=K, K=K, S_cap=1024), seed=77)
+    d = _dev(t)
+    pipe = mla.CapturedHostPipeline(B, K, d["kv_cache"], d["pe_cache"], d["wkv_b"])
+    x = U.oracle_inputs(t)
+    for i in range(n):
+        f = float(i + 1) * (-1) ** i              # a different query per step
+        h = pipe.host_inputs(i)
+        h["q_nope"].copy_((t["q_nope"].float() * f).to(torch.bfloat16))
+        for name in ("q_pe", "topk_idx", "end_pos"):
+            h[name].copy_(t[name])
+        pipe.submit()
+        pipe.finish()
+        torch.cuda.synchronize()
+        pipe.check_status()
+        out = pipe.host_output(i)
+        assert out.dtype == torch.bfloat16 and out.is_pinned()
+        x["q_nope"] = synth.to_f64(h["q_nope"])
+        ora = U.oracle_out(x, list(range(B)))
+        # bf16 head outputs: the attention tolerance plus one bf16 rounding
+        got = out.double().numpy()
+        U.assert_attn_close(got, ora, f"captured pipeline step {i}")
