@@ -53,6 +53,12 @@
 // raises m rescales O (after PV(j-1)), and each keeps its own running sum,
 // brought to the current m when it sees m change.
 //
+// Softmax warpgroups take blocks in turn (NWG of them; two, the measured
+// best: three with four gather warps ran slower).  Every barrier a warpgroup
+// waits on for its own blocks is indexed by the block's warpgroup (j % NWG,
+// phase j / NWG), so each waiter sees the phases of its barrier strictly in
+// order.
+//
 // Exchange ring without credits: block i is sent only after the peer's
 // block i-1 has been received here and PV(i-2) has finished reading P(i-2)
 // from slot (i-2) mod 3; the peer sends block i-1 only after it has consumed
@@ -82,16 +88,24 @@ constexpr int QROPE = H * 64;                // rotary part of Q_r: 128 heads x 
 constexpr int SEND = RECV;                   // this CTA's partial scores of one block, shipped by bulk copy
 constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_CAP * 4 + SEND + 1024;
 constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 384, TMEM_COLS = 512;   // S buffer k at S_COL + 64 k
-constexpr int THREADS = 640;
-constexpr int GATHER_THREADS = 256;          // warps 0-7
-constexpr int CPT = NK * 36 / GATHER_THREADS;   // 9 chunks per gather thread per block
+constexpr int THREADS = 640;                 // 20 warps
+constexpr int NWG = 2;                       // softmax warpgroups, taking blocks in turn
+constexpr int GATHER_WARPS = 16 - 4 * NWG;   // the rest of the 20 warps, after the MMA warpgroup
+constexpr int GATHER_THREADS = 32 * GATHER_WARPS;
+constexpr int CPT = NK * 36 / GATHER_THREADS;   // 16-byte chunks per gather thread per block
 static_assert(CPT * GATHER_THREADS == NK * 36, "chunks must divide evenly");
-constexpr int QK_WARP = 8, PV_WARP = 9, COPY_WARP = 10;
-constexpr int SOFTMAX_WARP0 = 12;            // warps 12-19: two warpgroups
+constexpr int QK_WARP = GATHER_WARPS, PV_WARP = GATHER_WARPS + 1, COPY_WARP = GATHER_WARPS + 2;
+constexpr int SOFTMAX_WARP0 = GATHER_WARPS + 4;
 constexpr int WG_THREADS = 128;
-// registers per thread after reallocation: 256*72 + 128*56 + 256*136 <= 640*96
-constexpr int REG_GATHER = 72, REG_MMA = 56, REG_SOFTMAX = 136;
-static_assert(256 * REG_GATHER + 128 * REG_MMA + 256 * REG_SOFTMAX <= THREADS * 96, "register split");
+static_assert(NRECV == NWG || NWG == 2, "with three warpgroups each owns one receive slot");
+// registers per thread after reallocation, within the launch's 640 x 96
+constexpr int REG_GATHER = NWG == 3 ? 80 : 72, REG_MMA = NWG == 3 ? 40 : 56, REG_SOFTMAX = NWG == 3 ? 120 : 136;
+static_assert(GATHER_THREADS * REG_GATHER + 128 * REG_MMA + NWG * WG_THREADS * REG_SOFTMAX <= THREADS * 96,
+              "register split");
+// latent columns of O_r that warpgroup w normalises and writes: [ocol(w), ocol(w+1))
+__host__ __device__ constexpr int ocol(int w) { return 16 * ((16 * w) / NWG); }
+// fp32 staging pitch of warpgroup w's part of a row: its 16-byte chunks rounded up to whole swizzle groups of 8
+__host__ __device__ constexpr int stage_row_bytes(int w) { return ((((ocol(w + 1) - ocol(w)) * 4 / 16) + 7) / 8) * 8 * 16; }
 constexpr float RESCALE_T = 8.f;             // lazy-max threshold (log2 units)
 constexpr float SCORE_RANGE = 2048.f;        // largest partial score sent without MLA_DEV_SCORE_RANGE
 
@@ -115,9 +129,15 @@ struct Params {
 
 struct Bars {
     uint64_t full[NS], empty[NS];
-    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], q_ready;
+    // Barriers a warpgroup waits on for its own blocks are kept per warpgroup
+    // (index j % NWG, phase j / NWG): a warpgroup then waits every phase of
+    // its barrier in order, and a parity wait can never refer to a phase two
+    // behind or ahead.  s_free is waited by the QK issuer alone, in order.
+    uint64_t s_full[NWG], pv_done[NWG], s_free[2], q_ready;
+    uint64_t p_full[NWG];  // P of warpgroup w's blocks (one barrier per warpgroup: with three, the
+                           // warpgroups of blocks j and j+2 differ and must not share a phase)
     uint64_t recv_full[NRECV];
-    uint64_t m_ready[2];   // m after block j is in mval[j % 2]
+    uint64_t m_ready[NWG]; // m after block j is in mval[j % 2] (phase j / NWG of m_ready[j % NWG])
     uint64_t l_ready;      // both running sums are in lsum (the send buffer, after the last copy)
     uint64_t send_ready;   // the send buffer holds block j's partial scores
     uint64_t drain[2];     // MMA issuers (QK, PV): every MMA they issued has completed
@@ -203,14 +223,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bars.full[s], GATHER_THREADS), mbar_init(&bars.empty[s], 1);
         for (int k = 0; k < 2; ++k) {
-            mbar_init(&bars.s_full[k], 1);
             mbar_init(&bars.s_free[k], WG_THREADS);
+        }
+        for (int k = 0; k < NWG; ++k) {
             mbar_init(&bars.p_full[k], WG_THREADS);
+            mbar_init(&bars.s_full[k], 1);
             mbar_init(&bars.pv_done[k], 1);
             mbar_init(&bars.m_ready[k], WG_THREADS);
         }
-        mbar_init(&bars.q_ready, 2 * WG_THREADS);
-        mbar_init(&bars.l_ready, 2 * WG_THREADS);
+        mbar_init(&bars.q_ready, NWG * WG_THREADS);
+        mbar_init(&bars.l_ready, NWG * WG_THREADS);
         mbar_init(&bars.send_ready, WG_THREADS);
         mbar_init(&bars.drain[0], 1);
         mbar_init(&bars.drain[1], 1);
@@ -232,9 +254,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     const uint32_t tmem = bars.tmem_base;
     const Deadline deadline = make_deadline(p.wait_ns);
 
-    if (warp < 8) {
+    if (warp < GATHER_WARPS) {
         // ------------------------------------------------------------ gather producers
-        // Chunk ch = tid + 256 q (q < 9) of a block belongs to key ch / 36;
+        // Chunk ch = tid + GATHER_THREADS q (q < CPT) of a block belongs to key ch / 36;
         // chunks 0..31 of a key are its latent half (4 atom columns x 8,
         // 128-byte swizzle), 32..35 its rotary half (64-byte swizzle).
         // Unselected keys are zero-filled.
@@ -307,13 +329,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                     for (int kk = 0; kk < 2; ++kk)
                         mma_ss(sc, smem_desc(qr + kk * 32, 16, 512, 4), smem_desc(base + STAGE_KV + kk * 32, 16, 512, 4),
                                idesc_qk, 1);
-                    mma_commit(&bars.s_full[k]);
+                    mma_commit(&bars.s_full[j % NWG]);
                 }
             } else {
                 constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
                 for (int j = 0; ok && j < nblk; ++j) {
-                    const int s = j % NS, k = j & 1;
-                    ok = wait_until(&bars.p_full[k], (j >> 1) & 1, deadline);
+                    const int s = j % NS;
+                    ok = wait_until(&bars.p_full[j % NWG], (j / NWG) & 1, deadline);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t base = smem_u32(stages + s * STAGE);
@@ -322,7 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                     for (int kk = 0; kk < NK / 16; ++kk)
                         mma_ss(tmem + O_COL, smem_desc(pa + kk * 32, 16, 1024, 2),
                                smem_desc(base + kk * 2048, NK * 128, 1024, 2), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bars.pv_done[k]);
+                    mma_commit(&bars.pv_done[j % NWG]);
                     mma_commit(&bars.empty[s]);
                 }
             }
@@ -351,8 +373,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         }
     } else {
-        // ------------------------------------------------------------ softmax warpgroups (ping-pong)
-        // warpgroup w handles blocks j = w, w+2, ...; thread = head h, all 64 keys
+        // ------------------------------------------------------------ softmax warpgroups (in turn)
+        // warpgroup w handles blocks j = w, w+NWG, ...; thread = head h, all 64 keys
         regs_inc<REG_SOFTMAX>();
         const int w = (warp - SOFTMAX_WARP0) >> 2;
         const int quad = warp & 3;
@@ -365,10 +387,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         grid_dep_wait();
         if (nblk > 0) {
             // Q_r: latent [256r, 256r+256) -> TMEM as 128 bf16 pairs (warpgroup w
-            // stores 16-column groups 4w .. 4w+3); rotary [32r, 32r+32) -> shared
-            // memory, K-major with the 64-byte swizzle (warpgroup 1)
+            // stores 16-column groups 8w/NWG .. 8(w+1)/NWG - 1); rotary [32r, 32r+32)
+            // -> shared memory, K-major with the 64-byte swizzle (warpgroup 1)
             const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + h) * QL);
-            for (int c0 = 4 * w; c0 < 4 * w + 4; ++c0) {
+            for (int c0 = (8 * w) / NWG; c0 < (8 * (w + 1)) / NWG; ++c0) {
                 uint32_t v[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -391,13 +413,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         const float sl2 = p.scale_log2;
         float m_mine = -INFINITY;   // m after this warpgroup's previous block
         float l = 0.f;              // this warpgroup's running sum, relative to m_mine
-        for (int j = w; j < nblk && ok; j += 2) {
+        for (int j = w; j < nblk && ok; j += NWG) {
             const int k = j & 1;
             const uint32_t sc = trow + S_COL + 64 * k;
             // validity of the block's keys (bit i of vlo / vhi: key i / 32 + i)
             const uint32_t vlo = __ballot_sync(0xffffffffu, sidx[j * NK + lane] >= 0);
             const uint32_t vhi = __ballot_sync(0xffffffffu, sidx[j * NK + 32 + lane] >= 0);
-            if (!warp_wait(&bars.s_full[k], (j >> 1) & 1, deadline)) { ok = false; break; }
+            if (!warp_wait(&bars.s_full[w], (j / NWG) & 1, deadline)) { ok = false; break; }
             tc_fence_after();
             float x[64];
             {
@@ -431,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 ok = false;
                 break;
             }
-            if (j >= 2 && !warp_wait(&bars.pv_done[k], ((j - 2) >> 1) & 1, deadline)) {
+            if (j >= 2 && !warp_wait(&bars.pv_done[(j - 2) % NWG], ((j - 2) / NWG) & 1, deadline)) {
                 ok = false;
                 break;
             }
@@ -485,12 +507,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             // running maximum: m after block j-1 comes from the other warpgroup
             float m_prev = -INFINITY;
             if (j >= 1) {
-                if (!warp_wait(&bars.m_ready[(j - 1) & 1], ((j - 1) >> 1) & 1, deadline)) { ok = false; break; }
+                if (!warp_wait(&bars.m_ready[(j - 1) % NWG], ((j - 1) / NWG) & 1, deadline)) { ok = false; break; }
                 m_prev = bars.mval[(j - 1) & 1][h];
             }
             const float m = bm > m_prev + RESCALE_T ? bm : m_prev;
             bars.mval[k][h] = m;
-            mbar_arrive(&bars.m_ready[k]);
+            mbar_arrive(&bars.m_ready[w]);
             // bring this warpgroup's sum to m
             if (m != m_mine) {
                 l = m_mine == -INFINITY ? 0.f : l * ex2(m_mine - m);
@@ -515,7 +537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             // raising m rescales O, after PV(j-1) has added its block
             if (__any_sync(0xffffffffu, m != m_prev && m_prev != -INFINITY)) {
                 const float f = (m != m_prev && m_prev != -INFINITY) ? ex2(m_prev - m) : 1.f;
-                if (!warp_wait(&bars.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, deadline)) { ok = false; break; }
+                if (!warp_wait(&bars.pv_done[(j - 1) % NWG], ((j - 1) / NWG) & 1, deadline)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < 256; c0 += 16) {
@@ -539,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars.p_full[k]);
+            mbar_arrive(&bars.p_full[w]);
         }
 
         // ------------------------------------------------------------ final sums and epilogue
@@ -547,7 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         float m_fin = -INFINITY, lt = 0.f;
         if (ok && nblk > 0) {
             const int jl = nblk - 1;
-            if (!warp_wait(&bars.m_ready[jl & 1], (jl >> 1) & 1, deadline)) ok = false;
+            if (!warp_wait(&bars.m_ready[jl % NWG], (jl / NWG) & 1, deadline)) ok = false;
             if (ok) {
                 m_fin = bars.mval[jl & 1][h];
                 const float lw = (m_mine == -INFINITY || m_fin == -INFINITY) ? 0.f : l * ex2(m_mine - m_fin);
@@ -557,13 +579,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 lsum[w * H + h] = lw;
                 mbar_arrive(&bars.l_ready);
                 if (!warp_wait(&bars.l_ready, 0, deadline)) ok = false;
-                lt = lsum[h] + lsum[H + h];
-                if (ok && !warp_wait(&bars.pv_done[jl & 1], (jl >> 1) & 1, deadline)) ok = false;
+                lt = 0.f;
+#pragma unroll
+                for (int v = 0; v < NWG; ++v) lt += lsum[v * H + h];
+                if (ok && !warp_wait(&bars.pv_done[jl % NWG], (jl / NWG) & 1, deadline)) ok = false;
                 tc_fence_after();
             }
         }
         if (!ok) fail(p);
-        // warpgroup w normalises columns [128 w, 128 w + 128) of O_r.  The rows
+        // warpgroup w normalises columns [ocol(w), ocol(w+1)) of O_r.  The rows
         // leave TMEM one head per thread; they are staged in shared memory (the
         // gather stages, idle once the last PV has completed) and then written
         // out by whole rows, so that every global store is coalesced.
@@ -571,38 +595,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         const bool have = tload && lt > 0.f;
         const float inv = have ? 1.f / lt : 0.f;
         const bool bf16_out = p.n_split == 1 && p.o_b16;
-        const int rowb = bf16_out ? 256 : 512;       // bytes of this warpgroup's part of one row
-        const uint32_t stg = smem_u32(stages) + w * (H * 512);
-        const uint32_t srow = stg + h * rowb;
+        const int cw0 = ocol(w), ncol = ocol(w + 1) - cw0;
+        const int esz = bf16_out ? 2 : 4;
+        const int nch = ncol * esz / 16;                 // 16-byte chunks of this warpgroup's part of a row
+        const int pitch_ch = (nch + 7) & ~7;             // staging row pitch in chunks (swizzle groups of 8)
+        constexpr int STG_REGION = STAGE * NS / NWG;     // staging bytes per warpgroup
+        static_assert(stage_row_bytes(NWG - 1) * H <= STG_REGION && stage_row_bytes(0) * H <= STG_REGION,
+                      "the staged rows of a warpgroup fit in its share of the gather stages");
+        const uint32_t stg = smem_u32(stages) + w * STG_REGION;
+        const uint32_t srow = stg + h * pitch_ch * 16;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t v0[16], v1[16];
+        for (int c0 = 0; c0 < ncol; c0 += 16) {
+            uint32_t v0[16];
             if (tload) {
-                tmem_ld16(trow + O_COL + 128 * w + c0, v0);
-                tmem_ld16(trow + O_COL + 128 * w + c0 + 16, v1);
+                tmem_ld16(trow + O_COL + cw0 + c0, v0);
                 tmem_ld_wait();
             }
-            float o[32];
+            float o[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                o[q] = have ? __uint_as_float(v0[q]) * inv : 0.f;
-                o[16 + q] = have ? __uint_as_float(v1[q]) * inv : 0.f;
-            }
+            for (int q = 0; q < 16; ++q) o[q] = have ? __uint_as_float(v0[q]) * inv : 0.f;
+            // chunk c of the row sits at (c & ~7) | ((c ^ h) & 7)
             if (bf16_out) {
-                // 32 columns = 4 chunks of 16 bytes; chunk c of the row sits at c ^ (h & 7)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = c0 / 8 + i;
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(srow + ((c ^ (h & 7)) << 4)),
+                for (int i = 0; i < 2; ++i) {
+                    const int c = c0 / 8 + i, pc = (c & ~7) | ((c ^ h) & 7);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(srow + (pc << 4)),
                                  "r"(pack_bf16(o[8 * i], o[8 * i + 1])), "r"(pack_bf16(o[8 * i + 2], o[8 * i + 3])),
                                  "r"(pack_bf16(o[8 * i + 4], o[8 * i + 5])), "r"(pack_bf16(o[8 * i + 6], o[8 * i + 7]))
                                  : "memory");
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c = c0 / 4 + i;
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(srow + ((c ^ (h & 7)) << 4)),
+                for (int i = 0; i < 4; ++i) {
+                    const int c = c0 / 4 + i, pc = (c & ~7) | ((c ^ h) & 7);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(srow + (pc << 4)),
                                  "f"(o[4 * i]), "f"(o[4 * i + 1]), "f"(o[4 * i + 2]), "f"(o[4 * i + 3])
                                  : "memory");
                 }
@@ -610,19 +636,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         }
         asm volatile("bar.sync %0, %1;" ::"r"(1 + w), "r"(WG_THREADS) : "memory");
         {
-            const int col0 = 256 * r + 128 * w;
-            const int nch = rowb / 16;                 // 16-byte chunks per row part
+            const int col0 = 256 * r + cw0;
             const size_t row0 = bf16_out || p.n_split == 1 ? (size_t)b * H : (size_t)unit * H;
             uint8_t *dst = bf16_out ? reinterpret_cast<uint8_t *>(p.o_b16 + row0 * C + col0)
                                     : reinterpret_cast<uint8_t *>((p.n_split == 1 ? p.o_out : p.part_o) + row0 * C + col0);
             const size_t pitch = bf16_out ? C * 2 : C * 4;   // bytes between the rows of two heads
 #pragma unroll 4
             for (int idx = wtid; idx < H * nch; idx += WG_THREADS) {
-                const int row = idx / nch, c = idx % nch;
+                const int row = idx / nch, c = idx % nch, pc = (c & ~7) | ((c ^ row) & 7);
                 uint32_t a0, a1, a2, a3;
                 asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                              : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                             : "r"(stg + row * rowb + ((c ^ (row & 7)) << 4)));
+                             : "r"(stg + (row * pitch_ch + pc) * 16));
                 *reinterpret_cast<uint4 *>(dst + row * pitch + c * 16) = make_uint4(a0, a1, a2, a3);
             }
         }
