@@ -523,6 +523,41 @@ def measure_workload(mla, synth, name: str, dev, flush, args, rank: int, world: 
     return rec, d, t, wl, step, graph
 
 
+def measure_fused_step(mla, synth, d, B, K, rows, flush, seed: int, n: int = 50, dim: int = 7168) -> dict:
+    """The attention block's whole decode step for one new token per sequence
+    (FusedDecodeStep: wkv_a projection, cache append, absorption, attention
+    with the up-projection, wo projection) on the bench caches, captured in
+    one CUDA graph; each replay timed with L2 flushed before it.  The model
+    width 7168 is the DeepSeek-V3 value (the pages leave dim out)."""
+    dev = d["kv_cache"].device
+    x, wkv_a = synth.make_linear_inputs(seed + 11, B, 576, dim, name="fused/wkv_a")
+    _, wo = synth.make_linear_inputs(seed + 12, 1, dim, 128 * 128, name="fused/wo")
+    x, wkv_a, wo = x.to(dev), wkv_a.to(dev), wo.to(dev)
+    norm_w = torch.ones(512, dtype=torch.float32, device=dev)
+    step = mla.FusedDecodeStep(B, K, dim, device=dev)
+    g = mla.CapturedStep(step, x, d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], wkv_a, norm_w, d["wkv_b"],
+                         wo, d["topk_idx"], d["end_pos"])
+    for i in range(3):
+        flush(i)
+        g()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        flush(i + 17)
+        ev[2 * i].record()
+        g()
+        ev[2 * i + 1].record()
+    torch.cuda.synchronize()
+    step.check_status()
+    ms = statistics.mean(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n))
+    nbytes = (wkv_a.numel() + wo.numel() + d["wkv_b"].numel() + x.numel()) * 2 + rows * ROW_BYTES + \
+        B * (576 * 2 + 1152) + B * dim * 2
+    return {"workload": f"B={B} new tokens, dim {dim}, top-{K} over the bench caches: wkv_a -> cache append -> "
+                        f"absorb -> attention + up-projection -> wo, one graph replay",
+            "kernel_ms": ms, "kernels_per_step": g.kernels_per_replay, "alg_bytes_per_launch": nbytes,
+            "achieved_gbs": nbytes / (ms * 1e-3) / 1e9}
+
+
 def run_ours(args):
     from sparse_latent_attention_decode_b300 import mla, synth
 
@@ -592,6 +627,8 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     next_rows = measure_next_rows(mla, synth, dev, flush, args.seed, n=args.next_steps)
+    next_rows["fused_step"] = measure_fused_step(mla, synth, d, B, K, rec["selected_rows"], flush, args.seed,
+                                                 n=args.next_steps)
     if B % 2 == 0:
         next_rows["multi_token_decode"] = measure_multi_token(mla, step, d, B, K, rec["selected_rows"], flush,
                                                               n=args.next_steps)

@@ -725,9 +725,18 @@ size_t attn_workspace(int B, int K, int *n_split_out, int *split_len_out) {
     return units * H * C * sizeof(float) + units * 2 * H * sizeof(float);
 }
 
+void attn_partials(int B, int K, void *ws, float **part_o, float **part_lse, int *n_split) {
+    int n = 1, len = K;
+    attn_workspace(B, K, &n, &len);
+    *n_split = n;
+    const size_t units = (size_t)B * n;
+    *part_o = n > 1 ? static_cast<float *>(ws) : nullptr;
+    *part_lse = n > 1 ? static_cast<float *>(ws) + units * H * C : nullptr;
+}
+
 int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, int S_cap, const int32_t *topk, int K,
                 const int32_t *end_pos, int B, int T, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
-                int32_t *status, cudaStream_t s, int *launches) {
+                int32_t *status, cudaStream_t s, int *launches, bool merge_later) {
     int n_split = 1, split_len = K;
     attn_workspace(B, K, &n_split, &split_len);
     attn::Params p{};
@@ -772,7 +781,7 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
         return MLA_ERR_CUDA;
     if (timed && cudaEventRecord(hook.stop, s) != cudaSuccess) return MLA_ERR_CUDA;
     int n = 1;
-    if (n_split > 1) {
+    if (n_split > 1 && !merge_later) {
         if (launch_k(!timed, attn::combine_kernel, dim3(B, H), dim3(128), 0, s, (const float *)p.part_o,
                      (const float *)p.part_lse, n_split, o_out, o_b16) != cudaSuccess)
             return MLA_ERR_CUDA;

@@ -68,13 +68,27 @@ extern "C" int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *k
     // with wkv_b the latent o goes through the workspace (bf16) to the up-projection
     uint16_t *o_b16 = wkv_b ? reinterpret_cast<uint16_t *>(ws + L.o_lat) : out_b16;
     int launches = 0;
+    // With wkv_b, one or two query rows and a split selection, the
+    // up-projection merges the split partials itself: no combine kernel and no
+    // bf16 o round trip, which at this size is mostly launch latency.  With
+    // more rows each up-projection CTA (one per head) would merge many rows in
+    // turn, and the parallel combine kernel is faster (measured at B = 16, 32).
+    const bool merge_in_up = wkv_b && B <= 2;
     int rc = launch_attn(q_lat, kv_cache, pe_cache, S_cap, topk_idx, K, end_pos, B, T, softmax_scale,
-                         wkv_b ? nullptr : out_f32, o_b16, ws + L.attn, dev_status, s, &launches);
+                         wkv_b ? nullptr : out_f32, o_b16, ws + L.attn, dev_status, s, &launches, merge_in_up);
     count_launches(launches);
     if (rc != MLA_OK) return rc;
     const ProfileHook &hook = profile_hook();
     const bool pdl = !(hook.start && hook.stop);
-    if (wkv_b) return launch_out_up(nullptr, o_b16, wkv_b, B, out_f32, out_b16, dev_status, s, pdl);
+    if (wkv_b) {
+        float *part_o = nullptr, *part_lse = nullptr;
+        int n_split = 1;
+        attn_partials(B, K, ws + L.attn, &part_o, &part_lse, &n_split);
+        if (merge_in_up && n_split > 1)
+            return launch_out_up(nullptr, nullptr, wkv_b, B, out_f32, out_b16, dev_status, s, pdl, part_o, part_lse,
+                                 n_split);
+        return launch_out_up(nullptr, o_b16, wkv_b, B, out_f32, out_b16, dev_status, s, pdl);
+    }
     return MLA_OK;
 }
 

@@ -11,8 +11,11 @@ namespace mla {
 // fp32 (o_f32, the standalone entry point) or as bf16 (o_b16, written by the
 // attention path); exactly one of them is non-NULL.  The head outputs go to
 // out (fp32) or, when out_b16 is non-NULL, to out_b16 (bf16).
+// With part_o non-NULL (and o_f32, o_b16 NULL) the operand is merged from
+// the attention kernel's split partials (part_o, part_lse, n_split per row).
 int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
-                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl);
+                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl, const float *part_o = nullptr,
+                  const float *part_lse = nullptr, int n_split = 0);
 
 // Sparse attention (tensor-core kernel + split combine) over B query rows,
 // T per sequence: row b is token b % T of cache sequence b / T, at position
@@ -21,9 +24,14 @@ int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv
 // bf16 to o_b16 (exactly one non-NULL).  ws must hold attn_workspace(B, K)
 // bytes (256-byte aligned).
 size_t attn_workspace(int B, int K, int *n_split = nullptr, int *split_len = nullptr);
+// With merge_later set and the selection split, the split-combine kernel is
+// not launched: the partials stay in ws (attn_partials) for the consumer.
 int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, int S_cap, const int32_t *topk, int K,
                 const int32_t *end_pos, int B, int T, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
-                int32_t *status, cudaStream_t s, int *launches);
+                int32_t *status, cudaStream_t s, int *launches, bool merge_later = false);
+// Where the split partials of launch_attn(B, K) live in its workspace
+// (part_o [B*n_split][128][512], part_lse [B*n_split][2][128]); n_split 1: none.
+void attn_partials(int B, int K, void *ws, float **part_o, float **part_lse, int *n_split);
 
 // Launch `kern` on stream s.  With pdl set, the launch allows programmatic
 // dependent launch: the grid may be scheduled while the preceding grid of the

@@ -64,9 +64,47 @@ __device__ __forceinline__ void stage_f32(const float *__restrict__ o_lat, int h
     }
 }
 
+// Split partials of one pass -> bf16 operand tile: each query row's latent
+// output o is merged from its n_split partials (normalised o of every split,
+// and the log2 of each split's softmax mass, one per latent half and head)
+// exactly as the split-combine kernel does, then rounded to bf16.
+__device__ __forceinline__ void stage_partials(const float *__restrict__ part_o, const float *__restrict__ part_lse,
+                                               int n_split, int h, int n0, int nb, int N, uint8_t *sB, int tid) {
+    const int total = N * 64;
+    for (int u = tid; u < total; u += 128) {
+        const int row = u >> 6, ch = u & 63, half = ch >= 32 ? 1 : 0;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+        if (row < nb) {
+            const size_t u0 = (size_t)(n0 + row) * n_split;
+            float M = -INFINITY;
+            for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, part_lse[((u0 + sp) * 2 + half) * H + h]);
+            float L = 0.f;
+            if (M != -INFINITY) {
+                for (int sp = 0; sp < n_split; ++sp) {
+                    const float lse = part_lse[((u0 + sp) * 2 + half) * H + h];
+                    if (lse == -INFINITY) continue;
+                    const float w = exp2f(lse - M);
+                    L += w;
+                    const float4 *src = reinterpret_cast<const float4 *>(part_o + ((u0 + sp) * H + h) * C + ch * 8);
+                    const float4 v0 = src[0], v1 = src[1];
+                    a.x = fmaf(w, v0.x, a.x), a.y = fmaf(w, v0.y, a.y), a.z = fmaf(w, v0.z, a.z), a.w = fmaf(w, v0.w, a.w);
+                    c.x = fmaf(w, v1.x, c.x), c.y = fmaf(w, v1.y, c.y), c.z = fmaf(w, v1.z, c.z), c.w = fmaf(w, v1.w, c.w);
+                }
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            a.x *= inv, a.y *= inv, a.z *= inv, a.w *= inv;
+            c.x *= inv, c.y *= inv, c.z *= inv, c.w *= inv;
+        }
+        *reinterpret_cast<uint4 *>(sB + (ch >> 3) * B_ATOM + sw128(row, ch & 7)) =
+            make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(c.x, c.y), pack_bf16(c.z, c.w));
+    }
+}
+
 __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ CUtensorMap wmap,
                                                         const __grid_constant__ CUtensorMap omap,
                                                         const float *__restrict__ o_f32, bool o_is_b16, int B,
+                                                        const float *__restrict__ part_o,
+                                                        const float *__restrict__ part_lse, int n_split,
                                                         float *__restrict__ out, uint16_t *__restrict__ out_b16,
                                                         int32_t *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -112,6 +150,9 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
                 for (int a = 0; a < 8; ++a) tma_load_3d(smem_u32(sB + a * B_ATOM), &omap, 64 * a, h, n0, &bars.b_full);
                 b_issued = pass + 1;
             }
+        } else if (part_o) {
+            stage_partials(part_o, part_lse, n_split, h, n0, nb, N, sB, tid);
+            fence_proxy_async_smem();
         } else {
             stage_f32(o_f32, h, n0, nb, N, sB, tid);
             fence_proxy_async_smem();
@@ -179,7 +220,8 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
 }  // namespace outup
 
 int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
-                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl) {
+                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl, const float *part_o,
+                  const float *part_lse, int n_split) {
     CUtensorMap wmap, omap;
     {
         const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H * WROWS};
@@ -205,7 +247,8 @@ int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     const cudaError_t err = launch_k(pdl, outup::out_up_kernel, dim3(H), dim3(128), outup::SMEM_BYTES, s, wmap,
-                                     omap, o_f32, o_b16 != nullptr, B, out, out_b16, status, wait_limit_ns());
+                                     omap, o_f32, o_b16 != nullptr, B, part_o, part_lse, n_split, out, out_b16, status,
+                                     wait_limit_ns());
     count_launches(1);
     return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

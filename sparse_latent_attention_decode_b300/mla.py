@@ -608,3 +608,57 @@ class CapturedHostPipeline:
     def check_status(self):
         for st in self.steps:
             st.check_status()
+
+
+class FusedDecodeStep:
+    """The attention block's decode step for one new token per sequence, from
+    the token's hidden state to the block's output, as five library calls on
+    the current stream (capture it with CapturedStep to make it one launch):
+
+        kv_a = x . wkv_a^T                       (mla_linear_bf16, bf16 out)
+        cache rows at end_pos - 1                (mla_cache_append: RMSNorm of
+                                                  the latent, rotation of the
+                                                  rotary key)
+        q_lat = [q_nope . W_UK | rope(q_pe)]     (mla_absorb_q)
+        heads = softmax over the selection . V, up-projected (mla_sparse_decode_tokens, bf16 out)
+        y = heads.flatten . wo^T                 (mla_linear_bf16)
+
+    x [B, dim] bf16 (the normalised hidden state), wkv_a [576, dim],
+    kv_norm_w [512] fp32, wo [dim, 16384] bf16; the query parts q_nope / q_pe
+    come from the query path, which needs trained weights and is not part of
+    this library.  end_pos counts the new token (its row is written at
+    end_pos - 1 before the attention reads the caches)."""
+
+    def __init__(self, B: int, K: int, dim: int, device="cuda", params: RopeParams | None = None,
+                 eps: float = 1e-6):
+        self.B, self.K, self.dim, self.eps = B, K, dim, eps
+        self.device = torch.device(device)
+        self.params = params if params is not None else rope_params()
+        self.scale = softmax_scale(self.params)
+        self.cis = rope_freqs_init(self.params, device=self.device)
+        dev = self.device
+        self.kv_a = torch.empty(B, Q_LAT, dtype=torch.bfloat16, device=dev)
+        self.q_lat = torch.empty(B, N_HEADS, Q_LAT, dtype=torch.bfloat16, device=dev)
+        self.heads = torch.empty(B, 1, N_HEADS, D_V, dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty(B, dim, dtype=torch.bfloat16, device=dev)
+        self.ws_attn = torch.empty(workspace_size(B, K), dtype=torch.uint8, device=dev)
+        self.ws_a = torch.empty(linear_workspace_size(B, Q_LAT, dim), dtype=torch.uint8, device=dev)
+        self.ws_o = torch.empty(linear_workspace_size(B, dim, N_HEADS * D_V), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def __call__(self, x, q_nope, q_pe, kv_cache, pe_cache, wkv_a, kv_norm_w, wkv_b, wo, topk_idx, end_pos):
+        mla_linear_bf16(x, wkv_a, out_dtype=torch.bfloat16, out=self.kv_a, workspace=self.ws_a,
+                        dev_status=self.status)
+        mla_cache_append(self.kv_a[:, None], kv_norm_w, self.cis, end_pos, kv_cache, pe_cache, eps=self.eps,
+                         dev_status=self.status)
+        mla_absorb_q(q_nope, q_pe, self.cis, end_pos, wkv_b, out=self.q_lat, dev_status=self.status)
+        mla_sparse_decode_tokens(self.q_lat[:, None], kv_cache, pe_cache, topk_idx[:, None], end_pos, self.scale,
+                                 wkv_b=wkv_b, out=self.heads, workspace=self.ws_attn, dev_status=self.status,
+                                 out_dtype=torch.bfloat16)
+        return mla_linear_bf16(self.heads.view(self.B, N_HEADS * D_V), wo, out_dtype=torch.bfloat16, out=self.y,
+                               workspace=self.ws_o, dev_status=self.status)
+
+    def check_status(self):
+        v = int(self.status.item())
+        if v:
+            raise MLAError(f"device status: {status_string(v)} (bits {v})")

@@ -406,6 +406,22 @@ def test_decode_with_fp8_wkv_b_matches_oracle():
 
 
 # ----------------------------------------------------------------- captured step
+def test_one_sequence_step_merges_its_splits_in_the_up_projection():
+    # B = 1: the selection is split over many units and the up-projection
+    # merges the partials itself (no combine kernel)
+    B, K = 1, 4096
+    t = synth.make_inputs(synth.small_workload(B, [4096], k=K, K=K, S_cap=4096, selection="all"), seed=43)
+    d = _dev(t)
+    step = mla.DecodeStep(B, K)
+    with mla.ProfileHook() as hook:
+        out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
+        torch.cuda.synchronize()
+    step.check_status()
+    assert hook.launches == 3                     # absorb, attention, up-projection
+    x = U.oracle_inputs(t)
+    U.assert_attn_close(out.cpu().numpy(), U.oracle_out(x, [0]), "one sequence, split merged in the up-projection")
+
+
 def test_captured_step_replays_the_eager_step_exactly():
     B, K = 5, 512
     t = synth.make_inputs(synth.small_workload(B, [900, 512, 1000, 64, 777], k=K, K=K, S_cap=1024), seed=41)
@@ -415,7 +431,8 @@ def test_captured_step_replays_the_eager_step_exactly():
     with mla.ProfileHook() as hook:
         eager = step(*args).clone()
     g = mla.CapturedStep(step, *args)
-    # absorb, attention, (split combine: 5 sequences do not fill the GPU,) up-projection
+    # absorb, attention, split combine (5 sequences do not fill the GPU: their
+    # selections are split), up-projection
     assert g.kernels_per_replay == hook.launches == 4
     d["q_nope"].mul_(-1)                      # new inputs in the captured buffers
     out = g().clone()
@@ -717,3 +734,60 @@ def test_captured_host_pipeline_steps_match_their_inputs():
         # bf16 head outputs: the attention tolerance plus one bf16 rounding
         got = out.double().numpy()
         U.assert_attn_close(got, ora, f"captured pipeline step {i}")
+
+
+def test_fused_decode_step_matches_the_oracle_chain():
+    # one new token per sequence, from its hidden state to the block output:
+    # wkv_a projection -> cache append -> absorption -> attention with the
+    # up-projection -> wo projection, eager and captured in one graph
+    B, K, S, dim = 4, 256, 1024, 1024
+    ends = [301, 513, 1001, 4]                    # counts the new token
+    t = synth.make_inputs(synth.small_workload(B, ends, k=K, K=K, S_cap=S), seed=97)
+    t["topk_idx"][:, 0] = t["end_pos"] - 1          # the new token is selected
+    x, wkv_a = synth.make_linear_inputs(98, B, 576, dim, name="wkv_a")
+    _, wo = synth.make_linear_inputs(99, 1, dim, 128 * 128, name="wo")
+    g = torch.Generator().manual_seed(100)
+    norm_w = (1.0 + 0.1 * torch.randn(512, generator=g)).to(torch.bfloat16).float()
+    d = _dev(t)
+    kv0, pe0 = d["kv_cache"].clone(), d["pe_cache"].clone()
+    dx, dwa, dwo, dnw = x.cuda(), wkv_a.cuda(), wo.cuda(), norm_w.cuda()
+    step = mla.FusedDecodeStep(B, K, dim)
+    args = (dx, d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], dwa, dnw, d["wkv_b"], dwo, d["topk_idx"],
+            d["end_pos"])
+    y = step(*args).clone()
+    torch.cuda.synchronize()
+    step.check_status()
+    # the oracle chain, rounding to bf16 where the path stores bf16 (the kv_a
+    # projection, the cache rows, the head outputs)
+    xo = U.oracle_inputs(t)
+    kv_a = O.round_to_bf16(O.linear(synth.to_f64(x), synth.to_f64(wkv_a)))
+    pos, lat, rot = O.cache_rows(kv_a[:, None], norm_w.double().numpy(), 1e-6, xo["end_pos"], U.INV_FREQ)
+    kvc, pec = xo["kv_cache"].copy(), xo["pe_cache"].copy()
+    for b in range(B):
+        kvc[b, pos[b, 0]] = O.round_to_bf16(lat[b, 0])
+        pec[b, pos[b, 0]] = O.round_to_bf16(rot[b, 0])
+    heads = O.decode_step(xo["q_nope"], xo["q_pe"], kvc, pec, xo["wkv_b"], xo["topk_idx"], xo["end_pos"],
+                          U.INV_FREQ, U.SCALE)
+    wod = synth.to_f64(wo)
+    ora = O.output_projection(O.round_to_bf16(heads), wod)
+    mag = O.output_projection(np.abs(heads), np.abs(wod))
+    err = np.abs(y.cpu().double().numpy() - ora)
+    # the attention tolerance carried through wo: an element of a sequence's
+    # head outputs may be off by 2e-2 of that sequence's largest head output,
+    # and the errors sum to at most 5e-3 of the outputs' magnitude; plus the
+    # bf16 rounding of y (2^-9 relative)
+    maxh = np.abs(heads).reshape(B, -1).max(axis=1)
+    bound = 2e-2 * maxh[:, None] * np.abs(wod).sum(axis=1)[None, :] + 2.0 ** -8 * np.abs(ora) + 1e-4
+    assert np.all(err <= bound), float(np.max(err / bound))
+    assert err.sum() / mag.sum() <= 5e-3 + 2.0 ** -9, float(err.sum() / mag.sum())
+    # the same step captured in one CUDA graph replays to the same result
+    d["kv_cache"].copy_(kv0)
+    d["pe_cache"].copy_(pe0)
+    gstep = mla.CapturedStep(step, *args)
+    d["kv_cache"].copy_(kv0)
+    d["pe_cache"].copy_(pe0)
+    yg = gstep().clone()
+    torch.cuda.synchronize()
+    step.check_status()
+    assert torch.equal(yg, y)
+    assert gstep.kernels_per_replay >= 5
