@@ -75,7 +75,7 @@ __device__ __forceinline__ void rope_part(const uint16_t *__restrict__ q_pe, con
     }
 }
 
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 4)
     absorb_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap qmap,
                   const uint16_t *__restrict__ q_pe, const float2 *__restrict__ cis, int max_seq_len,
                   const int32_t *__restrict__ end_pos, int B, int T, int nmax, uint16_t *__restrict__ q_lat,
@@ -86,12 +86,25 @@ __global__ void __launch_bounds__(128)
     uint8_t *sA = smem, *sB = smem + 2 * A_BOX;
     const int t = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    const int bbox = nmax * 128;   // bytes of one [nmax b][64 d] box of q_nope
+    const int npass = (B + nmax - 1) / nmax;
+    int b_issued = 0;   // batch tiles whose loads tid 0 has issued
     if (tid == 0) {
         mbar_init(&bars.a_full, 1);
         mbar_init(&bars.b_full, 1);
         mbar_init(&bars.mma_done, 1);
         mbar_init(&bars.drain, 1);
         fence_mbar_init();
+        // the copies go out first, before the TMEM allocation and the CTA barrier:
+        // W_UK[h] = rows h*256 .. h*256+127 of wkv_b, this tile = latent columns
+        // 128t .. 128t+127; then the first batch tile of q_nope
+        mbar_expect_tx(&bars.a_full, 2 * A_BOX);
+        tma_load_2d(smem_u32(sA), &wmap, 128 * t, h * WROWS, &bars.a_full);
+        tma_load_2d(smem_u32(sA + A_BOX), &wmap, 128 * t + 64, h * WROWS, &bars.a_full);
+        mbar_expect_tx(&bars.b_full, 2 * bbox);
+        tma_load_3d(smem_u32(sB), &qmap, 0, h, 0, &bars.b_full);
+        tma_load_3d(smem_u32(sB + bbox), &qmap, 64, h, 0, &bars.b_full);
+        b_issued = 1;
     }
     if (warp == 0) {
         tmem_alloc(&bars.tmem_base, NMAX);
@@ -105,22 +118,12 @@ __global__ void __launch_bounds__(128)
     const uint32_t tmem = bars.tmem_base;
     const Deadline deadline = make_deadline(wait_ns);
     bool ok = true;
-    int b_issued = 0;   // batch tiles whose loads tid 0 has issued
 
-    if (tid == 0) {
-        // W_UK[h] = rows h*256 .. h*256+127 of wkv_b; this tile = latent columns 128t .. 128t+127
-        mbar_expect_tx(&bars.a_full, 2 * A_BOX);
-        tma_load_2d(smem_u32(sA), &wmap, 128 * t, h * WROWS, &bars.a_full);
-        tma_load_2d(smem_u32(sA + A_BOX), &wmap, 128 * t + 64, h * WROWS, &bars.a_full);
-    }
-
-    const int bbox = nmax * 128;   // bytes of one [nmax b][64 d] box of q_nope
-    const int npass = (B + nmax - 1) / nmax;
     for (int pass = 0; pass < npass && ok; ++pass) {
         const int n0 = pass * nmax;
         const int nb = min(nmax, B - n0);
         const int N = (nb + 15) & ~15;
-        if (tid == 0) {
+        if (tid == 0 && pass > 0) {
             mbar_expect_tx(&bars.b_full, 2 * bbox);
             tma_load_3d(smem_u32(sB), &qmap, 0, h, n0, &bars.b_full);
             tma_load_3d(smem_u32(sB + bbox), &qmap, 64, h, n0, &bars.b_full);
@@ -147,19 +150,35 @@ __global__ void __launch_bounds__(128)
         ok = __syncthreads_and(wait_until(&bars.mma_done, pass & 1, deadline));
         if (!ok) break;
         tc_fence_after();
-        // epilogue: lane = latent column within the tile, column = sequence
-        const uint32_t trow = tmem + (uint32_t(32 * warp) << 16);
-        const int c = 128 * t + 32 * warp + lane;
-        for (int j0 = 0; j0 < N; j0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(trow + j0, v);
-            tmem_ld_wait();
+        // epilogue: lane = latent column within the tile, column = query row.  The
+        // rows are staged in shared memory over the batch tile (its MMAs have
+        // completed; row pitch 256 B, each warp writing 64 contiguous bytes of a
+        // row at a time) and leave as whole 256-byte row segments of q_lat.
+        {
+            const uint32_t trow = tmem + (uint32_t(32 * warp) << 16);
+            const uint32_t stg = smem_u32(sB) + (32 * warp + lane) * 2;
+            for (int j0 = 0; j0 < N; j0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(trow + j0, v);
+                tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int b = n0 + j0 + i;
-                if (b < B) q_lat[((size_t)b * H + h) * QL + c] = f2bf(__uint_as_float(v[i]));
+                for (int i = 0; i < 16; ++i)
+                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg + (j0 + i) * 256), "h"(f2bf(__uint_as_float(v[i])))
+                                 : "memory");
             }
         }
+        __syncthreads();
+        for (int idx = tid; idx < nb * 16; idx += 128) {
+            const int row = idx >> 4, ch = idx & 15;
+            uint32_t a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                         : "r"(smem_u32(sB) + row * 256 + ch * 16));
+            *reinterpret_cast<uint4 *>(q_lat + ((size_t)(n0 + row) * H + h) * QL + 128 * t + ch * 8) =
+                make_uint4(a0, a1, a2, a3);
+        }
+        // the next pass's batch tile overwrites the staging by TMA (async proxy)
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();   // TMEM and the batch tile are reused by the next pass
     }
