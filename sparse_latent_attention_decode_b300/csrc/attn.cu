@@ -170,7 +170,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, wait_until(bar, parity, deadline));
 }
 
-__device__ __forceinline__ float max4(float a, float b, float c, float d) { return fmaxf(fmaxf(a, b), fmaxf(c, d)); }
+// maximum of three (PTX max.f32 with three sources, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// lo_acc += the low fp16 half of w, hi_acc += the high half: PTX's mixed-precision
+// add widens the half exactly and rounds once, as a conversion and an fp32 add would
+__device__ __forceinline__ void add_f16x2(uint32_t w, float &lo_acc, float &hi_acc) {
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.f16 %0, lo, %0;\n add.rn.f32.f16 %1, hi, %1;\n}"
+        : "+f"(lo_acc), "+f"(hi_acc) : "r"(w));
+}
+
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_kernel(Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -442,10 +454,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             {
                 // the partial scores travel to the peer as fp16, rounded to 11 significant
                 // bits: flag magnitudes where that rounding reaches one unit of the raw score
-                float a[4] = {0.f, 0.f, 0.f, 0.f};
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                for (int q = 0; q < 64; ++q) a[q & 3] = fmaxf(a[q & 3], fabsf(x[q]));
-                if (fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])) > SCORE_RANGE) report(p.status, MLA_DEV_SCORE_RANGE);
+                for (int q = 0; q < 64; q += 4) {
+                    a0 = fmax3(a0, fabsf(x[q]), fabsf(x[q + 1]));
+                    a1 = fmax3(a1, fabsf(x[q + 2]), fabsf(x[q + 3]));
+                }
+                if (fmaxf(a0, a1) > SCORE_RANGE) report(p.status, MLA_DEV_SCORE_RANGE);
             }
             // ring credit: the peer's block j-1 has been received here (by the other
             // warpgroup), and PV(j-2) has read P(j-2) from its slot
@@ -483,9 +498,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                                  : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
                                  : "r"(src + ((c ^ (h & 7)) << 4)));
-                    const float2 f0 = unpack_f16(a0), f1 = unpack_f16(a1), f2 = unpack_f16(a2), f3 = unpack_f16(a3);
-                    x[8 * c] += f0.x, x[8 * c + 1] += f0.y, x[8 * c + 2] += f1.x, x[8 * c + 3] += f1.y;
-                    x[8 * c + 4] += f2.x, x[8 * c + 5] += f2.y, x[8 * c + 6] += f3.x, x[8 * c + 7] += f3.y;
+                    add_f16x2(a0, x[8 * c], x[8 * c + 1]);
+                    add_f16x2(a1, x[8 * c + 2], x[8 * c + 3]);
+                    add_f16x2(a2, x[8 * c + 4], x[8 * c + 5]);
+                    add_f16x2(a3, x[8 * c + 6], x[8 * c + 7]);
                 }
             }
             if ((vlo & vhi) != 0xffffffffu) {
@@ -497,12 +513,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             }
             float bm;
             {
-                float t[16];
+                float t[22], u[8];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) t[q] = max4(x[q], x[16 + q], x[32 + q], x[48 + q]);
+                for (int q = 0; q < 21; ++q) t[q] = fmax3(x[3 * q], x[3 * q + 1], x[3 * q + 2]);
+                t[21] = x[63];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) t[q] = max4(t[q], t[4 + q], t[8 + q], t[12 + q]);
-                bm = max4(t[0], t[1], t[2], t[3]) * sl2;   // raw scores -> log2 units (scale > 0)
+                for (int q = 0; q < 7; ++q) u[q] = fmax3(t[3 * q], t[3 * q + 1], t[3 * q + 2]);
+                u[7] = t[21];
+                bm = fmax3(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], u[5]), fmaxf(u[6], u[7])) * sl2;   // log2 units
             }
             // running maximum: m after block j-1 comes from the other warpgroup
             float m_prev = -INFINITY;

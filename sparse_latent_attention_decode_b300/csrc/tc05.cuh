@@ -368,13 +368,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
-__device__ __forceinline__ float2 unpack_f16(uint32_t v) {
-    float2 r;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "r"(v));
-    return r;
-}
 // 2^x (PTX ex2.approx, flush-to-zero); ex2(-inf) = +0
 __device__ __forceinline__ float ex2(float x) {
     float y;
