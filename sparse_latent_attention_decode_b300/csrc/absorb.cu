@@ -230,15 +230,8 @@ extern "C" int mla_absorb_q_tokens(const mla_bf16 *q_nope, const mla_bf16 *q_pe,
         if (!make_tmap_bf16(&qmap, q_nope, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(absorb::absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 absorb::SMEM_BYTES) != cudaSuccess)
-            return MLA_ERR_CUDA;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
+    static std::atomic<bool> smem_set[64];
+    if (!smem_attr_once(smem_set, absorb::absorb_kernel, absorb::SMEM_BYTES)) return MLA_ERR_CUDA;
     absorb::absorb_kernel<<<dim3(4, H), 128, absorb::smem_bytes(nmax), s>>>(
         wmap, qmap, q_pe, reinterpret_cast<const float2 *>(cis), max_seq_len, end_pos, B, T, nmax, q_lat, dev_status,
         wait_limit_ns());

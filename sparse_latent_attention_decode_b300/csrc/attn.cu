@@ -38,6 +38,7 @@
 //   warp 9      issues PV(j) once P(j) is in shared memory;
 //   warp 10     copies block j's partial scores to the peer once they are in
 //               the send buffer, and frees the buffer when the copy has read it;
+//   warp 11     forwards each completed PV(j) to the peer as a ring credit;
 //   warps 12-15 softmax of the even blocks, warps 16-19 of the odd blocks
 //               (ping-pong): one thread per head, all 64 keys of its block.
 // The selection of the unit (at most 2048 entries; longer selections are
@@ -59,12 +60,15 @@
 // phase j / NWG), so each waiter sees the phases of its barrier strictly in
 // order.
 //
-// Exchange ring without credits: block i is sent only after the peer's
-// block i-1 has been received here and PV(i-2) has finished reading P(i-2)
-// from slot (i-2) mod 3; the peer sends block i-1 only after it has consumed
-// block i-3 from the same slot (i mod 3) and PV(i-3) has read P(i-3) from
-// it.  The warpgroup that sends block i-1 is the one that received block
-// i-3, so that slot's previous mbarrier phase has completed too.
+// Exchange ring with direct credits: block i (i >= 3) is sent into the
+// peer's slot i mod 3 only after the peer's PV(i-3) has read P(i-3) from that
+// slot -- the peer's credit warp (warp 11) waits for each of its PVs and
+// arrives on this CTA's credit barrier of the slot.  The peer's copy of block
+// i then lands here after this CTA's own PV(i-3), and so after its softmax of
+// block i-3 has passed that slot's previous receive phase.  The warpgroup of
+// block i posts the receive barrier's byte count after the copy of block i-1
+// has read the send buffer, i.e. after the other warpgroup finished block
+// i-3.  Each CTA runs at most three blocks ahead of the other.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc05.cuh"
@@ -95,6 +99,7 @@ constexpr int GATHER_THREADS = 32 * GATHER_WARPS;
 constexpr int CPT = NK * 36 / GATHER_THREADS;   // 16-byte chunks per gather thread per block
 static_assert(CPT * GATHER_THREADS == NK * 36, "chunks must divide evenly");
 constexpr int QK_WARP = GATHER_WARPS, PV_WARP = GATHER_WARPS + 1, COPY_WARP = GATHER_WARPS + 2;
+constexpr int CREDIT_WARP = GATHER_WARPS + 3;
 constexpr int SOFTMAX_WARP0 = GATHER_WARPS + 4;
 constexpr int WG_THREADS = 128;
 static_assert(NRECV == NWG || NWG == 2, "with three warpgroups each owns one receive slot");
@@ -137,6 +142,8 @@ struct Bars {
     uint64_t p_full[NWG];  // P of warpgroup w's blocks (one barrier per warpgroup: with three, the
                            // warpgroups of blocks j and j+2 differ and must not share a phase)
     uint64_t recv_full[NRECV];
+    uint64_t credit[NRECV];   // the peer's PV(i) has read P(i) from its slot i mod 3 (phase i / 3), so
+                              // block i + 3 may be sent into it; arrived on by the peer's credit warp
     uint64_t m_ready[NWG]; // m after block j is in mval[j % 2] (phase j / NWG of m_ready[j % NWG])
     uint64_t l_ready;      // both running sums are in lsum (the send buffer, after the last copy)
     uint64_t send_ready;   // the send buffer holds block j's partial scores
@@ -249,7 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         mbar_init(&bars.drain[0], 1);
         mbar_init(&bars.drain[1], 1);
         bars.send_done = 0;
-        for (int k = 0; k < NRECV; ++k) mbar_init(&bars.recv_full[k], 1);
+        for (int k = 0; k < NRECV; ++k) mbar_init(&bars.recv_full[k], 1), mbar_init(&bars.credit[k], 1);
         fence_mbar_init();
     }
     if (warp == QK_WARP) {
@@ -365,6 +372,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             mma_commit(&bars.drain[warp - QK_WARP]);
             if (!wait_until(&bars.drain[warp - QK_WARP], 0, globaltimer_ns() + DRAIN_NS)) fail(p);
         }
+        if (lane == 0 && nblk > 0 && warp == CREDIT_WARP) {
+            // hands each completed PV(i) to the peer as the credit for its block i + 3
+            for (int i = 0; i + NRECV < nblk; ++i) {
+                if (!wait_until(&bars.pv_done[i % NWG], (i / NWG) & 1, deadline)) {
+                    fail(p);
+                    break;
+                }
+                mbar_arrive_cluster(&bars.credit[i % NRECV], peer);
+            }
+        }
         if (lane == 0 && nblk > 0 && warp == COPY_WARP) {
             // ships each block's partial scores to the peer's receive slot
             const uint32_t recv_peer = map_peer(smem_u32(recv), peer);
@@ -462,13 +479,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 }
                 if (fmaxf(a0, a1) > SCORE_RANGE) report(p.status, MLA_DEV_SCORE_RANGE);
             }
-            // ring credit: the peer's block j-1 has been received here (by the other
-            // warpgroup), and PV(j-2) has read P(j-2) from its slot
-            if (j >= 1 && !warp_wait(&bars.recv_full[(j - 1) % NRECV], ((j - 1) / NRECV) & 1, deadline)) {
-                ok = false;
-                break;
-            }
-            if (j >= 2 && !warp_wait(&bars.pv_done[(j - 2) % NWG], ((j - 2) / NWG) & 1, deadline)) {
+            // ring credit: the peer's PV(j-3) has read P(j-3) from its slot j mod 3.  The
+            // credit carries no data (the bulk copy that writes the slot is issued after
+            // this wait has seen the phase), so a CTA-scope wait is enough.
+            if (j >= NRECV && !warp_wait(&bars.credit[j % NRECV], ((j - NRECV) / NRECV) & 1, deadline)) {
                 ok = false;
                 break;
             }
@@ -780,15 +794,8 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
         p.part_o = static_cast<float *>(ws);
         p.part_lse = p.part_o + units * H * C;
     }
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(attn::attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, attn::SMEM_BYTES) !=
-            cudaSuccess)
-            return MLA_ERR_CUDA;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
+    static std::atomic<bool> smem_set[64];
+    if (!smem_attr_once(smem_set, attn::attn_kernel, attn::SMEM_BYTES)) return MLA_ERR_CUDA;
     const ProfileHook &hook = profile_hook();
     const bool timed = hook.start && hook.stop;
     // With the timing events in the stream the kernels are launched plainly:

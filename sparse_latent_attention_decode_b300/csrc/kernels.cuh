@@ -3,6 +3,8 @@
 
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace mla {
@@ -51,6 +53,20 @@ cudaError_t launch_k(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, si
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Raises kern's dynamic shared memory limit to `bytes` on the current device,
+// once per device: the flag is atomic, so calls from several host threads are
+// safe (two first calls may both set the attribute, which is harmless).
+template <typename Kern>
+bool smem_attr_once(std::atomic<bool> (&done)[64], Kern kern, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const bool cached = dev >= 0 && dev < 64;
+    if (cached && done[dev].load(std::memory_order_acquire)) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    if (cached) done[dev].store(true, std::memory_order_release);
+    return true;
 }
 
 // TMA tensor map of a bf16 tensor (dims[0] innermost); false on failure.

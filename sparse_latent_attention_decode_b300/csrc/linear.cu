@@ -246,15 +246,8 @@ extern "C" int mla_linear_bf16(const mla_bf16 *x, const mla_bf16 *w, int M, int 
         if (!make_tmap_bf16(&xmap, x, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
     }
     const int smem = lin::smem_bytes(NT);
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(lin::linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 lin::smem_bytes(lin::NT_MAX)) != cudaSuccess)
-            return MLA_ERR_CUDA;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
+    static std::atomic<bool> smem_set[64];
+    if (!smem_attr_once(smem_set, lin::linear_kernel, lin::smem_bytes(lin::NT_MAX))) return MLA_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     const dim3 grid((N + lin::BN - 1) / lin::BN, n_split, (M + NT - 1) / NT);
     float *part = n_split > 1 ? static_cast<float *>(workspace) : nullptr;

@@ -237,15 +237,8 @@ int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv
     } else {
         omap = wmap;   // unused
     }
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(outup::out_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 outup::SMEM_BYTES) != cudaSuccess)
-            return MLA_ERR_CUDA;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
+    static std::atomic<bool> smem_set[64];
+    if (!smem_attr_once(smem_set, outup::out_up_kernel, outup::SMEM_BYTES)) return MLA_ERR_CUDA;
     const cudaError_t err = launch_k(pdl, outup::out_up_kernel, dim3(H), dim3(128), outup::SMEM_BYTES, s, wmap,
                                      omap, o_f32, o_b16 != nullptr, B, part_o, part_lse, n_split, out, out_b16, status,
                                      wait_limit_ns());

@@ -63,16 +63,6 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(MBAR_SUSPEND_NS)
-        : "memory");
-    return ok != 0;
-}
 // Non-blocking probe: true when the phase with `parity` has completed.
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
@@ -82,18 +72,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
-}
-// Bounded wait: true when the phase with `parity` completed, false after
-// `limit` unsuccessful polls (each try_wait itself suspends for a while).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-    return false;
 }
 
 // ------------------------------------------------------------ fences
@@ -265,15 +243,6 @@ __device__ __forceinline__ bool wait_until(uint64_t *bar, uint32_t parity, const
         if (i >= 2) __nanosleep(i < 8 ? 32 : 96);
     }
 }
-__device__ __forceinline__ bool wait_until_cluster(uint64_t *bar, uint32_t parity, uint64_t deadline) {
-#pragma unroll 1
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (i >= 2) __nanosleep(i < 8 ? 32 : 96);
-        if ((i & 31) == 31 && globaltimer_ns() > deadline) return false;
-    }
-}
-
 // ------------------------------------------------------------ TMA
 // Gather four rows (row coordinates r0..r3, column start `col`) of a 2-D
 // tensor map whose box is one row high into consecutive rows at `dst`.
