@@ -15,11 +15,12 @@
 //         latent part of Q_r in TMEM and 2 with its rotary part in shared
 //         memory; B = the gathered tile, K-major.
 //   The two partial score tiles are exchanged through distributed shared
-//   memory and summed: each softmax warpgroup writes its CTA's raw scores as
-//   fp16 into a send buffer, and a copy warp ships the 16 KB with one bulk
-//   copy into a ring of three receive buffers in the peer, whose mbarriers
-//   count the arriving bytes.  Both CTAs then hold the full scores and run
-//   the same online softmax.
+//   memory and summed: each softmax warp writes its 32 heads' raw scores as
+//   fp16 into its quarter of a send buffer and ships that 4 KB quarter with
+//   its own bulk copy into a ring of three receive buffers in the peer, where
+//   one mbarrier per quarter counts the arriving bytes, so a warp waits only
+//   for its own heads' half of the scores.  Both CTAs then hold the full
+//   scores and run the same online softmax.
 //   PV  : O_r[128 heads, 256 latent] += P[128, 64] . V_r[64, 256]  (A = P
 //         as bf16 in shared memory, B = the same gathered tile read MN-major).
 // TMEM per CTA: O_r columns [0,256), latent Q_r [256,384), two score
@@ -36,9 +37,8 @@
 //   warp 8      issues QK(j) once stage j is full and score buffer j%2 has
 //               been read (block j-2);
 //   warp 9      issues PV(j) once P(j) is in shared memory;
-//   warp 10     copies block j's partial scores to the peer once they are in
-//               the send buffer, and frees the buffer when the copy has read it;
-//   warp 11     forwards each completed PV(j) to the peer as a ring credit;
+//   warp 11     forwards each completed PV(j) to the peer as a ring credit
+//               (warp 10 is idle);
 //   warps 12-15 softmax of the even blocks, warps 16-19 of the odd blocks
 //               (ping-pong): one thread per head, all 64 keys of its block.
 // The selection of the unit (at most 2048 entries; longer selections are
@@ -90,6 +90,7 @@ constexpr int RECV = H * NK * 2;             // fp16 partial scores of the peer,
 constexpr int IDX_CAP = 2048;                // selection entries of one unit staged in shared memory
 constexpr int QROPE = H * 64;                // rotary part of Q_r: 128 heads x 32 bf16 (64B swizzle)
 constexpr int SEND = RECV;                   // this CTA's partial scores of one block, shipped by bulk copy
+constexpr int QUARTER = RECV / 4;            // one warp's 32 rows of a block's scores, its own bulk copy
 constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_CAP * 4 + SEND + 1024;
 constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 384, TMEM_COLS = 512;   // S buffer k at S_COL + 64 k
 constexpr int THREADS = 640;                 // 20 warps
@@ -98,7 +99,7 @@ constexpr int GATHER_WARPS = 16 - 4 * NWG;   // the rest of the 20 warps, after 
 constexpr int GATHER_THREADS = 32 * GATHER_WARPS;
 constexpr int CPT = NK * 36 / GATHER_THREADS;   // 16-byte chunks per gather thread per block
 static_assert(CPT * GATHER_THREADS == NK * 36, "chunks must divide evenly");
-constexpr int QK_WARP = GATHER_WARPS, PV_WARP = GATHER_WARPS + 1, COPY_WARP = GATHER_WARPS + 2;
+constexpr int QK_WARP = GATHER_WARPS, PV_WARP = GATHER_WARPS + 1;
 constexpr int CREDIT_WARP = GATHER_WARPS + 3;
 constexpr int SOFTMAX_WARP0 = GATHER_WARPS + 4;
 constexpr int WG_THREADS = 128;
@@ -141,16 +142,15 @@ struct Bars {
     uint64_t s_full[NWG], pv_done[NWG], s_free[2], q_ready;
     uint64_t p_full[NWG];  // P of warpgroup w's blocks (one barrier per warpgroup: with three, the
                            // warpgroups of blocks j and j+2 differ and must not share a phase)
-    uint64_t recv_full[NRECV];
+    uint64_t recv_full[NRECV][4];   // quarter q (heads 32q .. 32q+31) of the peer's block in slot k
     uint64_t credit[NRECV];   // the peer's PV(i) has read P(i) from its slot i mod 3 (phase i / 3), so
                               // block i + 3 may be sent into it; arrived on by the peer's credit warp
     uint64_t m_ready[NWG]; // m after block j is in mval[j % 2] (phase j / NWG of m_ready[j % NWG])
     uint64_t l_ready;      // both running sums are in lsum (the send buffer, after the last copy)
-    uint64_t send_ready;   // the send buffer holds block j's partial scores
     uint64_t drain[2];     // MMA issuers (QK, PV): every MMA they issued has completed
-    int send_done;         // copies 0 .. send_done-1 have read the send buffer (a counter, not a
-                           // barrier: the warpgroup of block j waits for the copy of block j-1
-                           // without having seen the copy of block j-2 complete)
+    int send_done[4];      // copies 0 .. send_done[q]-1 of quarter q have read it from the send
+                           // buffer (a counter, not a barrier: the warp of block j waits for the
+                           // copy of block j-1 without having seen the copy of block j-2 complete)
     uint32_t tmem_base;
     float mval[2][H];
 };
@@ -252,11 +252,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         }
         mbar_init(&bars.q_ready, NWG * WG_THREADS);
         mbar_init(&bars.l_ready, NWG * WG_THREADS);
-        mbar_init(&bars.send_ready, WG_THREADS);
         mbar_init(&bars.drain[0], 1);
         mbar_init(&bars.drain[1], 1);
-        bars.send_done = 0;
-        for (int k = 0; k < NRECV; ++k) mbar_init(&bars.recv_full[k], 1), mbar_init(&bars.credit[k], 1);
+        for (int q = 0; q < 4; ++q) bars.send_done[q] = 0;
+        for (int k = 0; k < NRECV; ++k) {
+            for (int q = 0; q < 4; ++q) mbar_init(&bars.recv_full[k][q], 1);
+            mbar_init(&bars.credit[k], 1);
+        }
         fence_mbar_init();
     }
     if (warp == QK_WARP) {
@@ -382,25 +384,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 mbar_arrive_cluster(&bars.credit[i % NRECV], peer);
             }
         }
-        if (lane == 0 && nblk > 0 && warp == COPY_WARP) {
-            // ships each block's partial scores to the peer's receive slot
-            const uint32_t recv_peer = map_peer(smem_u32(recv), peer);
-            const uint32_t src = smem_u32(sendbuf);
-            for (int j = 0; j < nblk; ++j) {
-                if (!wait_until(&bars.send_ready, j & 1, deadline)) {
-                    fail(p);
-                    break;
-                }
-                const int kb = j % NRECV;
-                bulk_s2cluster(recv_peer + kb * RECV, src, SEND, map_peer(smem_u32(&bars.recv_full[kb]), peer));
-                bulk_commit();
-                bulk_wait_read();
-                *reinterpret_cast<volatile int *>(&bars.send_done) = j + 1;
-            }
-            // drain: every copy into the peer has been written before this CTA
-            // reaches the final cluster barrier (after which the peer may exit)
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        }
     } else {
         // ------------------------------------------------------------ softmax warpgroups (in turn)
         // warpgroup w handles blocks j = w, w+NWG, ...; thread = head h, all 64 keys
@@ -439,6 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             mbar_arrive(&bars.q_ready);
         }
         const uint32_t recv_local = smem_u32(recv);
+        const uint32_t recv_peer = map_peer(recv_local, peer);
         const float sl2 = p.scale_log2;
         float m_mine = -INFINITY;   // m after this warpgroup's previous block
         float l = 0.f;              // this warpgroup's running sum, relative to m_mine
@@ -488,9 +472,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             }
             {
                 const int kb = j % NRECV;
-                // this CTA's partial scores go to the send buffer (free once the copy of
-                // block j-1 has read it); the copy warp ships them to the peer's slot
-                if (!wait_count(&bars.send_done, j, deadline)) { ok = false; break; }
+                // this warp's 32 rows of partial scores go to its quarter of the send buffer
+                // (free once the copy of block j-1 -- the other warpgroup's warp of the same
+                // quarter -- has read it), and lane 0 ships the quarter to the peer's slot
+                if (!wait_count(&bars.send_done[quad], j, deadline)) { ok = false; break; }
                 const uint32_t sb = smem_u32(sendbuf) + h * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -501,10 +486,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                                  : "memory");
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars.send_ready);
-                // receive the peer's half of block j: this warpgroup announces the bytes
-                if (wtid == 0) mbar_expect_tx(&bars.recv_full[kb], RECV);
-                if (!warp_wait(&bars.recv_full[kb], (j / NRECV) & 1, deadline)) { ok = false; break; }
+                __syncwarp();
+                if (lane == 0) {
+                    // the peer's quarter of block j arrives here: this warp announces its bytes
+                    mbar_expect_tx(&bars.recv_full[kb][quad], QUARTER);
+                    bulk_s2cluster(recv_peer + kb * RECV + quad * QUARTER, smem_u32(sendbuf) + quad * QUARTER,
+                                   QUARTER, map_peer(smem_u32(&bars.recv_full[kb][quad]), peer));
+                    bulk_commit();
+                }
+                if (!warp_wait(&bars.recv_full[kb][quad], (j / NRECV) & 1, deadline)) { ok = false; break; }
+                if (lane == 0) {
+                    // the copy has long read the quarter by now: hand it to the next block's warp
+                    bulk_wait_read();
+                    *reinterpret_cast<volatile int *>(&bars.send_done[quad]) = j + 1;
+                }
                 const uint32_t src = recv_local + kb * RECV + h * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -596,6 +591,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             mbar_arrive(&bars.p_full[w]);
         }
 
+        // drain: every copy this lane issued into the peer has been written before the
+        // CTA reaches the final cluster barrier (after which the peer may exit)
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         // ------------------------------------------------------------ final sums and epilogue
         // m after the last block; both sums are brought to it and added
         float m_fin = -INFINITY, lt = 0.f;
@@ -606,8 +604,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 m_fin = bars.mval[jl & 1][h];
                 const float lw = (m_mine == -INFINITY || m_fin == -INFINITY) ? 0.f : l * ex2(m_mine - m_fin);
                 // the sums go to the send buffer once the last copy has read it
-                float *lsum = reinterpret_cast<float *>(sendbuf);
-                if (!wait_count(&bars.send_done, nblk, deadline)) ok = false;
+                float *lsum = reinterpret_cast<float *>(sendbuf);   // 1 KB: quarter 0 of the buffer
+                if (!wait_count(&bars.send_done[0], nblk, deadline)) ok = false;
                 lsum[w * H + h] = lw;
                 mbar_arrive(&bars.l_ready);
                 if (!warp_wait(&bars.l_ready, 0, deadline)) ok = false;
