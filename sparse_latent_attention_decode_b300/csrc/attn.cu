@@ -402,19 +402,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             // stores 16-column groups 8w/NWG .. 8(w+1)/NWG - 1); rotary [32r, 32r+32)
             // -> shared memory, K-major with the 64-byte swizzle (warpgroup 1)
             const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + h) * QL);
-            for (int c0 = (8 * w) / NWG; c0 < (8 * (w + 1)) / NWG; ++c0) {
+            // every load of the row is issued before the first store, so their latencies overlap
+            constexpr int QMAX = (8 + NWG - 1) / NWG;   // 16-column groups of a warpgroup, at most
+            const int g0 = (8 * w) / NWG, ng = (8 * (w + 1)) / NWG - g0;
+            uint4 qv[QMAX][4], qr[4];
+#pragma unroll
+            for (int i = 0; i < QMAX; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    qv[i][q] = i < ng ? qrow[(256 * r) / 8 + (g0 + i) * 4 + q] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) qr[c] = w == 1 ? qrow[(512 + 32 * r) / 8 + c] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < QMAX; ++i) {
+                if (i >= ng) break;
                 uint32_t v[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 x = qrow[(256 * r) / 8 + c0 * 4 + q];
-                    v[4 * q] = x.x, v[4 * q + 1] = x.y, v[4 * q + 2] = x.z, v[4 * q + 3] = x.w;
-                }
-                tmem_st16(trow + Q_COL + 16 * c0, v);
+                for (int q = 0; q < 4; ++q)
+                    v[4 * q] = qv[i][q].x, v[4 * q + 1] = qv[i][q].y, v[4 * q + 2] = qv[i][q].z, v[4 * q + 3] = qv[i][q].w;
+                tmem_st16(trow + Q_COL + 16 * (g0 + i), v);
             }
             if (w == 1) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(qrope + sw64(h, c)) = qrow[(512 + 32 * r) / 8 + c];
+                for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(qrope + sw64(h, c)) = qr[c];
                 fence_proxy_async_smem();
             }
             tmem_st_wait();
