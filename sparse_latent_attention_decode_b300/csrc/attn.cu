@@ -177,6 +177,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, wait_until(bar, parity, deadline));
 }
 
+// Bounded wait that polls without suspending: for the single-lane issuer
+// warps, which have nothing else to do and must act as soon as a phase completes.
+__device__ __forceinline__ bool wait_spin(uint64_t *bar, uint32_t parity, const Deadline &d) {
+#pragma unroll 1
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63) == 63 && globaltimer_ns() > d.t) return false;
+    }
+}
 // maximum of three (PTX max.f32 with three sources, sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
@@ -334,8 +343,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 for (int j = 0; ok && j < nblk; ++j) {
                     const int s = j % NS, k = j & 1;
                     // stage j gathered; score buffer k read by the softmax of block j-2
-                    ok = wait_until(&bars.full[s], (j / NS) & 1, deadline) &&
-                         (j < 2 || wait_until(&bars.s_free[k], ((j - 2) >> 1) & 1, deadline));
+                    ok = wait_spin(&bars.full[s], (j / NS) & 1, deadline) &&
+                         (j < 2 || wait_spin(&bars.s_free[k], ((j - 2) >> 1) & 1, deadline));
                     if (!ok) break;
                     // the stage was written by cp.async (generic proxy) and is read by the MMA (async proxy)
                     fence_proxy_async_smem();
@@ -356,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
                 for (int j = 0; ok && j < nblk; ++j) {
                     const int s = j % NS;
-                    ok = wait_until(&bars.p_full[j % NWG], (j / NWG) & 1, deadline);
+                    ok = wait_spin(&bars.p_full[j % NWG], (j / NWG) & 1, deadline);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t base = smem_u32(stages + s * STAGE);
@@ -377,7 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         if (lane == 0 && nblk > 0 && warp == CREDIT_WARP) {
             // hands each completed PV(i) to the peer as the credit for its block i + 3
             for (int i = 0; i + NRECV < nblk; ++i) {
-                if (!wait_until(&bars.pv_done[i % NWG], (i / NWG) & 1, deadline)) {
+                if (!wait_spin(&bars.pv_done[i % NWG], (i / NWG) & 1, deadline)) {
                     fail(p);
                     break;
                 }
