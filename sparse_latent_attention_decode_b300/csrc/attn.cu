@@ -41,10 +41,11 @@
 //               (warp 10 is idle);
 //   warps 12-15 softmax of the even blocks, warps 16-19 of the odd blocks
 //               (ping-pong): one thread per head, all 64 keys of its block.
-// The selection of the unit (at most 2048 entries; longer selections are
-// split across units) is staged in shared memory once (positions
+// The selection of the unit is staged in shared memory once (positions
 // outside [0, end_pos) become -1), so no global index load sits on the
-// per-block path.
+// per-block path: as 16-bit positions when the cache has at most 65,535 rows
+// (up to 4096 entries per unit), else as 32-bit ones (up to 2048); longer
+// selections are split across units.
 //
 // Online softmax with a lazy running maximum m (log2 units): block j's
 // maximum replaces m only when it exceeds m by more than 8, which keeps
@@ -65,10 +66,13 @@
 // slot -- the peer's credit warp (warp 11) waits for each of its PVs and
 // arrives on this CTA's credit barrier of the slot.  The peer's copy of block
 // i then lands here after this CTA's own PV(i-3), and so after its softmax of
-// block i-3 has passed that slot's previous receive phase.  The warpgroup of
-// block i posts the receive barrier's byte count after the copy of block i-1
-// has read the send buffer, i.e. after the other warpgroup finished block
-// i-3.  Each CTA runs at most three blocks ahead of the other.
+// block i-3 has passed that slot's previous receive phase.  The warp of block
+// i that owns a quarter posts that quarter's receive byte count after the
+// copy of block i-1's same quarter has read the send buffer, i.e. after the
+// other warpgroup's warp of that quarter finished block i-3.  Each CTA runs at
+// most three blocks ahead of the other.  The issuer lanes (QK, PV, credits)
+// poll their barriers rather than suspend: they have nothing else to do, and
+// the QK issuer's reaction to a landed stage is on every block's path.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tc05.cuh"
@@ -87,11 +91,13 @@ constexpr int STAGE_PE = NK * 64;            // 32 rotary columns x 64 keys (64B
 constexpr int STAGE = STAGE_KV + STAGE_PE;   // 36864
 constexpr int NRECV = 3;                     // exchange ring depth
 constexpr int RECV = H * NK * 2;             // fp16 partial scores of the peer, 128 x 64
-constexpr int IDX_CAP = 2048;                // selection entries of one unit staged in shared memory
+constexpr int IDX_BYTES = 8192;              // the unit's selection, staged in shared memory
+constexpr int IDX_CAP = IDX_BYTES / 4;       // entries as 32-bit positions
+constexpr int IDX_CAP16 = IDX_BYTES / 2;     // entries as 16-bit positions (caches of at most 65,535 rows)
 constexpr int QROPE = H * 64;                // rotary part of Q_r: 128 heads x 32 bf16 (64B swizzle)
 constexpr int SEND = RECV;                   // this CTA's partial scores of one block, shipped by bulk copy
 constexpr int QUARTER = RECV / 4;            // one warp's 32 rows of a block's scores, its own bulk copy
-constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_CAP * 4 + SEND + 1024;
+constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_BYTES + SEND + 1024;
 constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 384, TMEM_COLS = 512;   // S buffer k at S_COL + 64 k
 constexpr int THREADS = 640;                 // 20 warps
 constexpr int NWG = 2;                       // softmax warpgroups, taking blocks in turn
@@ -124,7 +130,7 @@ struct Params {
     int S_cap, K, B;    // B: query rows, T per sequence (row b is token b % T of sequence b / T)
     int T;
     float scale_log2;   // softmax_scale * log2(e)
-    int n_split, split_len;   // split_len <= IDX_CAP
+    int n_split, split_len;   // split_len <= IDX_CAP (32-bit staging) or IDX_CAP16 (16-bit)
     float *o_out;       // n_split == 1: normalised o, fp32 [B][128][512] (or NULL)
     uint16_t *o_b16;    // n_split == 1: normalised o, bf16 [B][128][512] (or NULL)
     float *part_o;      // n_split > 1: per-split normalised o, fp32 [B*n_split][128][512]
@@ -156,6 +162,19 @@ struct Bars {
 };
 
 __device__ __forceinline__ void fail(const Params &p) { report(p.status, MLA_DEV_TIMEOUT); }
+
+// Entry i of the staged selection: a position, or -1 for padding and positions
+// outside the row's visible range.  IDX16: 16-bit positions, 0xFFFF for none
+// (units of more than IDX_CAP entries, over caches of at most 65,535 rows).
+template <bool IDX16>
+__device__ __forceinline__ int sel_at(const int32_t *sidx, int i) {
+    if constexpr (IDX16) {
+        const uint32_t v = reinterpret_cast<const uint16_t *>(sidx)[i];
+        return v == 0xFFFFu ? -1 : int(v);
+    } else {
+        return sidx[i];
+    }
+}
 
 // Bounded wait until a shared-memory counter written by another thread of the
 // CTA reaches `target` (warp-uniform result).
@@ -200,6 +219,7 @@ __device__ __forceinline__ void add_f16x2(uint32_t w, float &lo_acc, float &hi_a
 }
 
 
+template <bool IDX16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_kernel(Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
@@ -208,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     uint8_t *recv = smem + NS * STAGE;
     uint8_t *qrope = recv + NRECV * RECV;
     int32_t *sidx = reinterpret_cast<int32_t *>(qrope + QROPE);
-    uint8_t *sendbuf = qrope + QROPE + IDX_CAP * 4;
+    uint8_t *sendbuf = qrope + QROPE + IDX_BYTES;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t r = cluster_rank(), peer = r ^ 1u;
@@ -244,7 +264,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int i = i0 + u * THREADS;
-                if (i < n) sidx[i] = (id[u] >= 0 && id[u] < e) ? id[u] : -1;
+                if (i < n) {
+                    const bool valid = id[u] >= 0 && id[u] < e;
+                    if constexpr (IDX16)
+                        reinterpret_cast<uint16_t *>(sidx)[i] = valid ? uint16_t(id[u]) : uint16_t(0xFFFFu);
+                    else
+                        sidx[i] = valid ? id[u] : -1;
+                }
             }
         }
     }
@@ -319,10 +345,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 break;
             }
             const uint32_t base = smem_u32(stages + s * STAGE);
-            const int32_t *bidx = sidx + j * NK;
+            const int bofs = j * NK;
 #pragma unroll
             for (int q = 0; q < CPT; ++q) {
-                const int id = bidx[key[q]];
+                const int id = sel_at<IDX16>(sidx, bofs + key[q]);
                 const size_t row = id < 0 ? 0 : (size_t)id;
                 const uint16_t *src = ((pe_mask >> q) & 1u) ? peb + row * DR + src_off[q] : kvb + row * C + src_off[q];
                 cp_async16(base + dst_off[q], src, id < 0 ? 0u : 16u);
@@ -449,8 +475,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             const int k = j & 1;
             const uint32_t sc = trow + S_COL + 64 * k;
             // validity of the block's keys (bit i of vlo / vhi: key i / 32 + i)
-            const uint32_t vlo = __ballot_sync(0xffffffffu, sidx[j * NK + lane] >= 0);
-            const uint32_t vhi = __ballot_sync(0xffffffffu, sidx[j * NK + 32 + lane] >= 0);
+            const uint32_t vlo = __ballot_sync(0xffffffffu, sel_at<IDX16>(sidx, j * NK + lane) >= 0);
+            const uint32_t vhi = __ballot_sync(0xffffffffu, sel_at<IDX16>(sidx, j * NK + 32 + lane) >= 0);
             if (!warp_wait(&bars.s_full[w], (j / NWG) & 1, deadline)) { ok = false; break; }
             tc_fence_after();
             float x[64];
@@ -752,18 +778,20 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
 }  // namespace attn
 
 // ------------------------------------------------------------------ host side
-int attn_n_split(int B, int K) {
+int attn_n_split(int B, int K, int S_cap) {
     const int pairs = 74;   // 148 SMs, one CTA pair per unit
     int n = B >= pairs ? 1 : pairs / B;
     const int max_split = (K + 127) / 128;
     if (n > max_split) n = max_split;
-    const int min_split = (K + attn::IDX_CAP - 1) / attn::IDX_CAP;   // a unit's selection fits in shared memory
+    // a unit's selection fits in shared memory (16-bit positions when the cache allows)
+    const int cap = S_cap <= 65535 ? attn::IDX_CAP16 : attn::IDX_CAP;
+    const int min_split = (K + cap - 1) / cap;
     if (n < min_split) n = min_split;
     return n < 1 ? 1 : n;
 }
 
-size_t attn_workspace(int B, int K, int *n_split_out, int *split_len_out) {
-    int n = attn_n_split(B, K);
+size_t attn_workspace(int B, int K, int *n_split_out, int *split_len_out, int S_cap) {
+    int n = attn_n_split(B, K, S_cap);
     int len = (K + n - 1) / n;
     len = (len + attn::NK - 1) / attn::NK * attn::NK;
     n = (K + len - 1) / len;
@@ -774,9 +802,9 @@ size_t attn_workspace(int B, int K, int *n_split_out, int *split_len_out) {
     return units * H * C * sizeof(float) + units * 2 * H * sizeof(float);
 }
 
-void attn_partials(int B, int K, void *ws, float **part_o, float **part_lse, int *n_split) {
+void attn_partials(int B, int K, int S_cap, void *ws, float **part_o, float **part_lse, int *n_split) {
     int n = 1, len = K;
-    attn_workspace(B, K, &n, &len);
+    attn_workspace(B, K, &n, &len, S_cap);
     *n_split = n;
     const size_t units = (size_t)B * n;
     *part_o = n > 1 ? static_cast<float *>(ws) : nullptr;
@@ -787,7 +815,7 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
                 const int32_t *end_pos, int B, int T, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
                 int32_t *status, cudaStream_t s, int *launches, bool merge_later) {
     int n_split = 1, split_len = K;
-    attn_workspace(B, K, &n_split, &split_len);
+    attn_workspace(B, K, &n_split, &split_len, S_cap);
     attn::Params p{};
     p.q_lat = q_lat;
     p.kv = kv;
@@ -801,6 +829,9 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.n_split = n_split;
     p.split_len = split_len;
+    // 16-bit staging only where a unit holds more entries than 32-bit staging fits (the
+    // split policy allows that only over caches of at most 65,535 rows)
+    const bool idx16 = split_len > attn::IDX_CAP;
     p.status = status;
     p.wait_ns = wait_limit_ns();
     if (n_split == 1) {
@@ -812,13 +843,15 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
         p.part_lse = p.part_o + units * H * C;
     }
     static std::atomic<bool> smem_set[64];
-    if (!smem_attr_once(smem_set, attn::attn_kernel, attn::SMEM_BYTES)) return MLA_ERR_CUDA;
+    static std::atomic<bool> smem_set16[64];
+    auto kern = idx16 ? attn::attn_kernel<true> : attn::attn_kernel<false>;
+    if (!smem_attr_once(idx16 ? smem_set16 : smem_set, kern, attn::SMEM_BYTES)) return MLA_ERR_CUDA;
     const ProfileHook &hook = profile_hook();
     const bool timed = hook.start && hook.stop;
     // With the timing events in the stream the kernels are launched plainly:
     // an event between two grids would separate them anyway.
     if (timed && cudaEventRecord(hook.start, s) != cudaSuccess) return MLA_ERR_CUDA;
-    if (launch_k(!timed, attn::attn_kernel, dim3(2 * B * n_split), dim3(attn::THREADS), attn::SMEM_BYTES, s, p) !=
+    if (launch_k(!timed, kern, dim3(2 * B * n_split), dim3(attn::THREADS), attn::SMEM_BYTES, s, p) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
     if (timed && cudaEventRecord(hook.stop, s) != cudaSuccess) return MLA_ERR_CUDA;

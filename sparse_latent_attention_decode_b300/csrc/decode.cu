@@ -83,7 +83,7 @@ extern "C" int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *k
     if (wkv_b) {
         float *part_o = nullptr, *part_lse = nullptr;
         int n_split = 1;
-        attn_partials(B, K, ws + L.attn, &part_o, &part_lse, &n_split);
+        attn_partials(B, K, S_cap, ws + L.attn, &part_o, &part_lse, &n_split);
         if (merge_in_up && n_split > 1)
             return launch_out_up(nullptr, nullptr, wkv_b, B, out_f32, out_b16, dev_status, s, pdl, part_o, part_lse,
                                  n_split);

@@ -25,15 +25,19 @@ int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv
 // Writes the normalised latent output o [B][128][512] as fp32 to o_out or as
 // bf16 to o_b16 (exactly one non-NULL).  ws must hold attn_workspace(B, K)
 // bytes (256-byte aligned).
-size_t attn_workspace(int B, int K, int *n_split = nullptr, int *split_len = nullptr);
+// The split of the selection (n_split units per row, split_len entries each)
+// depends on S_cap: caches of at most 65,535 rows stage 16-bit positions, so a
+// unit holds up to 4096 entries instead of 2048.  The default S_cap gives the
+// larger of the two workspaces, which covers every cache.
+size_t attn_workspace(int B, int K, int *n_split = nullptr, int *split_len = nullptr, int S_cap = 1 << 30);
 // With merge_later set and the selection split, the split-combine kernel is
 // not launched: the partials stay in ws (attn_partials) for the consumer.
 int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, int S_cap, const int32_t *topk, int K,
                 const int32_t *end_pos, int B, int T, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
                 int32_t *status, cudaStream_t s, int *launches, bool merge_later = false);
-// Where the split partials of launch_attn(B, K) live in its workspace
+// Where the split partials of launch_attn(B, K, S_cap) live in its workspace
 // (part_o [B*n_split][128][512], part_lse [B*n_split][2][128]); n_split 1: none.
-void attn_partials(int B, int K, void *ws, float **part_o, float **part_lse, int *n_split);
+void attn_partials(int B, int K, int S_cap, void *ws, float **part_o, float **part_lse, int *n_split);
 
 // Launch `kern` on stream s.  With pdl set, the launch allows programmatic
 // dependent launch: the grid may be scheduled while the preceding grid of the

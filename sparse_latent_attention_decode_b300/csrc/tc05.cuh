@@ -179,10 +179,6 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t cta) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
     return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -244,16 +240,6 @@ __device__ __forceinline__ bool wait_until(uint64_t *bar, uint32_t parity, const
     }
 }
 // ------------------------------------------------------------ TMA
-// Gather four rows (row coordinates r0..r3, column start `col`) of a 2-D
-// tensor map whose box is one row high into consecutive rows at `dst`.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *map, int col, int r0, int r1, int r2, int r3,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
-}
 // Tiled load of a 2-D / 3-D box at the given coordinates.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int c0, int c1, uint64_t *bar) {
     asm volatile(
@@ -279,23 +265,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ------------------------------------------------------------ asynchronous remote store (distributed shared memory)
-// 16 bytes into the shared memory of another CTA of the cluster; the bytes
-// are counted (complete_tx) on the mbarrier `cbar` of that same CTA.  Both
-// addresses are shared::cluster addresses (map_peer).
-__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
-                                            uint32_t cbar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
-                     caddr),
-                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(cbar)
-                 : "memory");
-}
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
 // shared memory of a CTA of the cluster; the destination mbarrier (in that

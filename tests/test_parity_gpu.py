@@ -155,6 +155,8 @@ SMALL = [
     (2, [1000, 1000], 1000, 1000, 1024, "all"),
     (4, [2100, 1500, 2048, 700], 1100, 1100, 2112, "recent_half"),
     (2, [5000, 4097], 2048, 2048, 5000, "uniform"),
+    (40, [4096] * 40, 4096, 4096, 4096, "uniform"),        # one unit of 4096 entries (16-bit staged positions)
+    (2, [70000, 65600], 3000, 3000, 70000, "uniform"),     # a cache of 70,000 rows: 32-bit staged positions
 ]
 
 
@@ -164,7 +166,9 @@ def test_sparse_decode_small_matches_oracle(case):
     t = synth.make_inputs(synth.small_workload(B, ep, k=k, K=K, S_cap=S, selection=sel), seed=3)
     d = _dev(t)
     x = U.oracle_inputs(t)
-    step = mla.DecodeStep(B, K)
+    # a rotary table long enough for the positions (its frequencies do not depend on its length)
+    params = mla.rope_params(max_seq_len=S) if S > 16384 else None
+    step = mla.DecodeStep(B, K, params=params)
     out = step(d["q_nope"], d["q_pe"], d["kv_cache"], d["pe_cache"], d["wkv_b"], d["topk_idx"], d["end_pos"])
     torch.cuda.synchronize()
     step.check_status()
