@@ -43,9 +43,10 @@
 //               (ping-pong): one thread per head, all 64 keys of its block.
 // The selection of the unit is staged in shared memory once (positions
 // outside [0, end_pos) become -1), so no global index load sits on the
-// per-block path: as 16-bit positions when the cache has at most 65,535 rows
-// (up to 4096 entries per unit), else as 32-bit ones (up to 2048); longer
-// selections are split across units.
+// per-block path: as 32-bit positions (up to 2048 entries per unit), or as
+// 16-bit ones when a unit holds more (up to 4096, which the split policy
+// allows only over caches of at most 65,535 rows); longer selections are
+// split across units.
 //
 // Online softmax with a lazy running maximum m (log2 units): block j's
 // maximum replaces m only when it exceeds m by more than 8, which keeps
