@@ -46,7 +46,9 @@
 // per-block path: as 32-bit positions (up to 2048 entries per unit), or as
 // 16-bit ones when a unit holds more (up to 4096, which the split policy
 // allows only over caches of at most 65,535 rows); longer selections are
-// split across units.
+// split across units.  A unit processes its blocks up to the one that holds
+// its last position: blocks of padding alone after it (a selection row
+// wider than the cached positions, early in a sequence) would add nothing.
 //
 // Online softmax with a lazy running maximum m (log2 units): block j's
 // maximum replaces m only when it exceeds m by more than 8, which keeps
@@ -159,10 +161,15 @@ struct Bars {
                            // buffer (a counter, not a barrier: the warp of block j waits for the
                            // copy of block j-1 without having seen the copy of block j-2 complete)
     uint32_t tmem_base;
+    int last_valid[THREADS / 32];   // per warp: the last staged entry that holds a position (-1: none)
+    int nblk;                       // blocks the unit processes (up to the one holding its last position)
     float mval[2][H];
 };
 
 __device__ __forceinline__ void fail(const Params &p) { report(p.status, MLA_DEV_TIMEOUT); }
+
+// blocks the unit processes, as published in shared memory before the cluster barrier
+__device__ __forceinline__ int unit_blocks(const Bars &bars) { return *reinterpret_cast<const volatile int *>(&bars.nblk); }
 
 // Entry i of the staged selection: a position, or -1 for padding and positions
 // outside the row's visible range.  IDX16: 16-bit positions, 0xFFFF for none
@@ -247,14 +254,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     const int e = e_seq - p.T + (b - cb * p.T) + 1;
     const int t0 = split * p.split_len;
     const int t1 = min(p.K, t0 + p.split_len);
-    const int nblk = (seq_ok && t1 > t0) ? (t1 - t0 + NK - 1) / NK : 0;
+    const int nblk_sel = (seq_ok && t1 > t0) ? (t1 - t0 + NK - 1) / NK : 0;   // blocks of the unit's selection
     if (!seq_ok && tid == 0 && r == 0 && split == 0) report(p.status, MLA_DEV_BAD_END_POS);
 
     // the unit's selection, padded to whole blocks; padding and positions
     // outside [0, end_pos) become -1 (four independent loads per thread)
     {
         const int32_t *sel = p.topk + (size_t)b * p.K;
-        const int n = nblk * NK;
+        const int n = nblk_sel * NK;
+        int last = -1;
         for (int i0 = tid; i0 < n; i0 += 4 * THREADS) {
             int id[4];
 #pragma unroll
@@ -267,6 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 const int i = i0 + u * THREADS;
                 if (i < n) {
                     const bool valid = id[u] >= 0 && id[u] < e;
+                    if (valid) last = i;
                     if constexpr (IDX16)
                         reinterpret_cast<uint16_t *>(sidx)[i] = valid ? uint16_t(id[u]) : uint16_t(0xFFFFu);
                     else
@@ -274,6 +283,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 }
             }
         }
+        // the unit's blocks end with the one that holds its last position: blocks of
+        // padding alone after it are not processed (they would add nothing)
+#pragma unroll
+        for (int off = 16; off; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+        if (lane == 0) bars.last_valid[warp] = last;
     }
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bars.full[s], GATHER_THREADS), mbar_init(&bars.empty[s], 1);
@@ -301,9 +315,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         tmem_alloc(&bars.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
+    __syncthreads();   // every warp's last staged position is in
+    if (tid == 0) {
+        // blocks to process (both CTAs of the pair stage the same selection and agree)
+        int last = -1;
+        for (int v = 0; v < THREADS / 32; ++v) last = max(last, bars.last_valid[v]);
+        bars.nblk = (last + NK) / NK;
+    }
     tc_fence_before();
     cluster_sync();   // barriers of both CTAs initialised, TMEM address published, selection staged
     tc_fence_after();
+    // the block count is read where it is used (from shared memory) rather than
+    // held in a register across the whole kernel
     // The dependent grid (value up-projection) may start its prologue now; it
     // reads this grid's output only after its own griddepcontrol.wait, which
     // returns once this grid -- and so the grid before it -- has completed.
@@ -339,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         }
         const uint16_t *kvb = p.kv + (size_t)cb * p.S_cap * C;
         const uint16_t *peb = p.pe + (size_t)cb * p.S_cap * DR;
-        for (int j = 0; j < nblk; ++j) {
+        for (int j = 0; j < unit_blocks(bars); ++j) {
             const int s = j % NS;
             if (j >= NS && !warp_wait(&bars.empty[s], ((j / NS) - 1) & 1, deadline)) {
                 fail(p);
@@ -361,13 +384,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     } else if (warp < SOFTMAX_WARP0) {
         // ------------------------------------------------------------ MMA issuers (warp 8: QK, warp 9: PV)
         regs_dec<REG_MMA>();
-        if (lane == 0 && nblk > 0 && (warp == QK_WARP || warp == PV_WARP)) {
+        if (lane == 0 && unit_blocks(bars) > 0 && (warp == QK_WARP || warp == PV_WARP)) {
             bool ok = true;
             if (warp == QK_WARP) {
                 constexpr uint32_t idesc_qk = idesc_bf16(128, NK, false, false);
                 ok = wait_until(&bars.q_ready, 0, deadline);
                 const uint32_t qr = smem_u32(qrope);
-                for (int j = 0; ok && j < nblk; ++j) {
+                for (int j = 0; ok && j < unit_blocks(bars); ++j) {
                     const int s = j % NS, k = j & 1;
                     // stage j gathered; score buffer k read by the softmax of block j-2
                     ok = wait_spin(&bars.full[s], (j / NS) & 1, deadline) &&
@@ -390,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 }
             } else {
                 constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
-                for (int j = 0; ok && j < nblk; ++j) {
+                for (int j = 0; ok && j < unit_blocks(bars); ++j) {
                     const int s = j % NS;
                     ok = wait_spin(&bars.p_full[j % NWG], (j / NWG) & 1, deadline);
                     if (!ok) break;
@@ -410,9 +433,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             mma_commit(&bars.drain[warp - QK_WARP]);
             if (!wait_until(&bars.drain[warp - QK_WARP], 0, globaltimer_ns() + DRAIN_NS)) fail(p);
         }
-        if (lane == 0 && nblk > 0 && warp == CREDIT_WARP) {
+        if (lane == 0 && unit_blocks(bars) > 0 && warp == CREDIT_WARP) {
             // hands each completed PV(i) to the peer as the credit for its block i + 3
-            for (int i = 0; i + NRECV < nblk; ++i) {
+            for (int i = 0; i + NRECV < unit_blocks(bars); ++i) {
                 if (!wait_spin(&bars.pv_done[i % NWG], (i / NWG) & 1, deadline)) {
                     fail(p);
                     break;
@@ -433,7 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         // q_lat comes from the preceding grid, and an earlier grid may still read
         // the buffers the epilogue writes: both wait for it to complete
         grid_dep_wait();
-        if (nblk > 0) {
+        if (unit_blocks(bars) > 0) {
             // Q_r: latent [256r, 256r+256) -> TMEM as 128 bf16 pairs (warpgroup w
             // stores 16-column groups 8w/NWG .. 8(w+1)/NWG - 1); rotary [32r, 32r+32)
             // -> shared memory, K-major with the 64-byte swizzle (warpgroup 1)
@@ -472,7 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         const float sl2 = p.scale_log2;
         float m_mine = -INFINITY;   // m after this warpgroup's previous block
         float l = 0.f;              // this warpgroup's running sum, relative to m_mine
-        for (int j = w; j < nblk && ok; j += NWG) {
+        for (int j = w; j < unit_blocks(bars) && ok; j += NWG) {
             const int k = j & 1;
             const uint32_t sc = trow + S_COL + 64 * k;
             // validity of the block's keys (bit i of vlo / vhi: key i / 32 + i)
@@ -643,15 +666,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         // ------------------------------------------------------------ final sums and epilogue
         // m after the last block; both sums are brought to it and added
         float m_fin = -INFINITY, lt = 0.f;
-        if (ok && nblk > 0) {
-            const int jl = nblk - 1;
+        if (ok && unit_blocks(bars) > 0) {
+            const int jl = unit_blocks(bars) - 1;
             if (!warp_wait(&bars.m_ready[jl % NWG], (jl / NWG) & 1, deadline)) ok = false;
             if (ok) {
                 m_fin = bars.mval[jl & 1][h];
                 const float lw = (m_mine == -INFINITY || m_fin == -INFINITY) ? 0.f : l * ex2(m_mine - m_fin);
                 // the sums go to the send buffer once the last copy has read it
                 float *lsum = reinterpret_cast<float *>(sendbuf);   // 1 KB: quarter 0 of the buffer
-                if (!wait_count(&bars.send_done[0], nblk, deadline)) ok = false;
+                if (!wait_count(&bars.send_done[0], unit_blocks(bars), deadline)) ok = false;
                 lsum[w * H + h] = lw;
                 mbar_arrive(&bars.l_ready);
                 if (!warp_wait(&bars.l_ready, 0, deadline)) ok = false;
@@ -667,7 +690,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         // leave TMEM one head per thread; they are staged in shared memory (the
         // gather stages, idle once the last PV has completed) and then written
         // out by whole rows, so that every global store is coalesced.
-        const bool tload = ok && nblk > 0;   // warp-uniform: tcgen05.ld is warp-collective
+        const bool tload = ok && unit_blocks(bars) > 0;   // warp-uniform: tcgen05.ld is warp-collective
         const bool have = tload && lt > 0.f;
         const float inv = have ? 1.f / lt : 0.f;
         const bool bf16_out = p.n_split == 1 && p.o_b16;
