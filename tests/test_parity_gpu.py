@@ -155,6 +155,7 @@ SMALL = [
     (2, [1000, 1000], 1000, 1000, 1024, "all"),
     (4, [2100, 1500, 2048, 700], 1100, 1100, 2112, "recent_half"),
     (2, [5000, 4097], 2048, 2048, 5000, "uniform"),
+    (3, [1000, 70, 3000], 2048, 2048, 3000, "uniform"),    # rows mostly padding: units cut short or left empty
     (40, [4096] * 40, 4096, 4096, 4096, "uniform"),        # one unit of 4096 entries (16-bit staged positions)
     (2, [70000, 65600], 3000, 3000, 70000, "uniform"),     # a cache of 70,000 rows: 32-bit staged positions
 ]
