@@ -469,11 +469,37 @@ class HostDecodeStep(DecodeStep):
                  out_dtype=torch.float32):
         super().__init__(B, K, device, params, out_dtype)
         dev = self.device
-        self.d_q_nope = torch.empty(B, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=dev)
-        self.d_q_pe = torch.empty(B, N_HEADS, D_ROPE, dtype=torch.bfloat16, device=dev)
-        self.d_topk = torch.empty(B, K, dtype=torch.int32, device=dev)
-        self.d_end = torch.empty(B, dtype=torch.int32, device=dev)
+        # the per-step inputs live in one device buffer (see packed_inputs), so that a
+        # caller holding them in one pinned buffer of the same layout copies them at once
+        self.d_packed = torch.empty(self.packed_bytes(B, K), dtype=torch.uint8, device=dev)
+        self.d_q_nope, self.d_q_pe, self.d_topk, self.d_end = self.packed_inputs(self.d_packed, B, K)
         self.h_out = torch.empty(B, N_HEADS, D_V, dtype=out_dtype).pin_memory()
+
+    @staticmethod
+    def _packed_layout(B: int, K: int):
+        sizes = (B * N_HEADS * D_NOPE * 2, B * N_HEADS * D_ROPE * 2, B * K * 4, B * 4)
+        offs, o = [], 0
+        for n in sizes:
+            offs.append(o)
+            o += (n + 255) // 256 * 256
+        return offs, o
+
+    @staticmethod
+    def packed_bytes(B: int, K: int) -> int:
+        """Bytes of one buffer holding a step's inputs (q_nope, q_pe, topk_idx,
+        end_pos, each at a 256-byte aligned offset)."""
+        return HostDecodeStep._packed_layout(B, K)[1]
+
+    @staticmethod
+    def packed_inputs(buf: torch.Tensor, B: int, K: int):
+        """Views (q_nope, q_pe, topk_idx, end_pos) into a uint8 buffer of
+        packed_bytes(B, K) bytes, host or device."""
+        offs, _ = HostDecodeStep._packed_layout(B, K)
+        q_nope = buf[offs[0]:offs[0] + B * N_HEADS * D_NOPE * 2].view(torch.bfloat16).view(B, N_HEADS, D_NOPE)
+        q_pe = buf[offs[1]:offs[1] + B * N_HEADS * D_ROPE * 2].view(torch.bfloat16).view(B, N_HEADS, D_ROPE)
+        topk = buf[offs[2]:offs[2] + B * K * 4].view(torch.int32).view(B, K)
+        end = buf[offs[3]:offs[3] + B * 4].view(torch.int32)
+        return q_nope, q_pe, topk, end
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in (self.d_q_nope, self.d_q_pe, self.d_topk, self.d_end))
@@ -486,6 +512,14 @@ class HostDecodeStep(DecodeStep):
         self.d_q_pe.copy_(h_q_pe, non_blocking=True)
         self.d_topk.copy_(h_topk, non_blocking=True)
         self.d_end.copy_(h_end, non_blocking=True)
+        out = self(self.d_q_nope, self.d_q_pe, kv_cache, pe_cache, wkv_b, self.d_topk, self.d_end)
+        self.h_out.copy_(out, non_blocking=True)
+        return self.h_out
+
+    def run_packed(self, h_packed, kv_cache, pe_cache, wkv_b):
+        """run() with the inputs in one pinned buffer laid out by packed_inputs:
+        one host-to-device copy instead of four."""
+        self.d_packed.copy_(h_packed, non_blocking=True)
         out = self(self.d_q_nope, self.d_q_pe, kv_cache, pe_cache, wkv_b, self.d_topk, self.d_end)
         self.h_out.copy_(out, non_blocking=True)
         return self.h_out
@@ -553,7 +587,7 @@ class HostDecodePipeline:
 class CapturedHostPipeline:
     """End-to-end decode steps from pinned host buffers, each step one CUDA
     graph replay: the graph copies the step's query parts, selection and
-    end_pos in from pinned host memory, runs absorption, attention and
+    end_pos in from one pinned host buffer (one copy), runs absorption, attention and
     up-projection, and copies the head outputs back into pinned host memory.
     Two buffer sets, each with its own graph and stream, alternate, so that
     one step's transfers overlap the other's compute, and the host makes one
@@ -569,12 +603,13 @@ class CapturedHostPipeline:
         self.steps, self.h_in, self.graphs, self.streams = [], [], [], []
         for _ in range(2):
             st = HostDecodeStep(B, K, self.device, params, out_dtype)
-            h = {"q_nope": torch.zeros(B, N_HEADS, D_NOPE, dtype=torch.bfloat16).pin_memory(),
-                 "q_pe": torch.zeros(B, N_HEADS, D_ROPE, dtype=torch.bfloat16).pin_memory(),
-                 "topk_idx": torch.full((B, K), -1, dtype=torch.int32).pin_memory(),
-                 "end_pos": torch.ones(B, dtype=torch.int32).pin_memory()}
-            g = CapturedStep(st.run, h["q_nope"], h["q_pe"], h["topk_idx"], h["end_pos"], kv_cache, pe_cache,
-                             wkv_b)
+            # the step's inputs in one pinned buffer: one host-to-device copy per step
+            packed = torch.zeros(HostDecodeStep.packed_bytes(B, K), dtype=torch.uint8).pin_memory()
+            q_nope, q_pe, topk, end = HostDecodeStep.packed_inputs(packed, B, K)
+            topk.fill_(-1)
+            end.fill_(1)
+            h = {"q_nope": q_nope, "q_pe": q_pe, "topk_idx": topk, "end_pos": end}
+            g = CapturedStep(st.run_packed, packed, kv_cache, pe_cache, wkv_b)
             self.steps.append(st)
             self.h_in.append(h)
             self.graphs.append(g)
@@ -588,7 +623,7 @@ class CapturedHostPipeline:
         return self.steps[i % 2].h_out
 
     def h2d_bytes(self):
-        return self.steps[0].h2d_bytes()
+        return self.steps[0].d_packed.numel()
 
     def d2h_bytes(self):
         return self.steps[0].d2h_bytes()

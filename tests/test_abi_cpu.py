@@ -120,3 +120,29 @@ def test_python_wrappers_reject_cpu_tensors():
     x = torch.zeros(1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mla.mla_rope_apply(x, torch.zeros(16, 32, 2), torch.ones(1, dtype=torch.int32))
+
+
+def test_packed_host_inputs_are_disjoint_aligned_views():
+    # the host pipeline copies a step's four inputs as one buffer: each view
+    # starts on a 256-byte boundary, has its tensor's shape and touches no other
+    import torch
+    B, K = 5, 300
+    n = mla.HostDecodeStep.packed_bytes(B, K)
+    buf = torch.zeros(n, dtype=torch.uint8)
+    q_nope, q_pe, topk, end = mla.HostDecodeStep.packed_inputs(buf, B, K)
+    assert q_nope.shape == (B, mla.N_HEADS, mla.D_NOPE) and q_nope.dtype == torch.bfloat16
+    assert q_pe.shape == (B, mla.N_HEADS, mla.D_ROPE) and q_pe.dtype == torch.bfloat16
+    assert topk.shape == (B, K) and topk.dtype == torch.int32
+    assert end.shape == (B,) and end.dtype == torch.int32
+    base = buf.data_ptr()
+    spans = []
+    for t in (q_nope, q_pe, topk, end):
+        off = t.data_ptr() - base
+        assert off % 256 == 0
+        spans.append((off, off + t.numel() * t.element_size()))
+    spans.sort()
+    assert spans[-1][1] <= n and all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+    for i, t in enumerate((q_nope, q_pe, topk, end)):
+        t.view(torch.uint8).fill_(i + 1)
+    assert int((buf == 1).sum()) == q_nope.numel() * 2
+    assert int((buf == 4).sum()) == end.numel() * 4
