@@ -254,7 +254,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     const int e = e_seq - p.T + (b - cb * p.T) + 1;
     const int t0 = split * p.split_len;
     const int t1 = min(p.K, t0 + p.split_len);
-    const int nblk_sel = (seq_ok && t1 > t0) ? (t1 - t0 + NK - 1) / NK : 0;   // blocks of the unit's selection
+    // blocks of the unit's selection: their loads do not wait for end_pos (a bad end_pos
+    // leaves every entry invalid and the unit empty), so the two latencies overlap
+    const int nblk_sel = t1 > t0 ? (t1 - t0 + NK - 1) / NK : 0;
     if (!seq_ok && tid == 0 && r == 0 && split == 0) report(p.status, MLA_DEV_BAD_END_POS);
 
     // the unit's selection, padded to whole blocks; padding and positions
@@ -274,7 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             for (int u = 0; u < 4; ++u) {
                 const int i = i0 + u * THREADS;
                 if (i < n) {
-                    const bool valid = id[u] >= 0 && id[u] < e;
+                    const bool valid = seq_ok && id[u] >= 0 && id[u] < e;
                     if (valid) last = i;
                     if constexpr (IDX16)
                         reinterpret_cast<uint16_t *>(sidx)[i] = valid ? uint16_t(id[u]) : uint16_t(0xFFFFu);
