@@ -40,7 +40,9 @@
  *  - Conditions only the device can see (an end_pos outside [1, S_cap], a
  *    position outside the rotary table, a bounded wait that ran out) are OR-ed
  *    as MLA_DEV_* bits into *dev_status (when dev_status is non-NULL); read it
- *    after synchronising the stream.  Affected sequences produce zeros.
+ *    after synchronising the stream.  Affected sequences produce zeros.  A
+ *    repeated position in a selection row is not detected on the decode path;
+ *    mla_check_selection finds it on request.
  */
 #ifndef MLA_DECODE_H
 #define MLA_DECODE_H
@@ -78,6 +80,8 @@ typedef struct CUstream_st *mla_stream_t; /* same type as cudaStream_t */
 #define MLA_DEV_SCORE_RANGE 8    /* a partial score exceeded 2048 in magnitude: the
                                     exchanged fp16 copy may be off by a whole unit
                                     (see mla_sparse_decode, precision) */
+#define MLA_DEV_DUPLICATE_INDEX 16 /* a selection row repeats a valid position
+                                      (set by mla_check_selection only) */
 
 /* Rotary / YaRN parameters.  Defaults (mla_rope_params_default) are those of
  * the "Transformer blocks" page, excerpt model-args: max_seq_len 16384,
@@ -239,6 +243,30 @@ int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, co
  *   o_lat [B][128][512] fp32, wkv_b [32768][512] bf16, out [B][128][128] fp32.
  * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096). */
 int mla_out_up(const float *o_lat, const mla_bf16 *wkv_b, int B, float *out, mla_stream_t stream);
+
+/* mla_check_selection -- validation of the selection rows, for callers that
+ * want to verify the distinct-positions precondition of mla_sparse_decode
+ * (a debugging aid: no other entry point calls it, and it is not needed for
+ * correct input).  The selection is a set ("Attention weights" page, excerpt
+ * mla-decode: zeros scattered into a row of -inf), while the attention
+ * kernels add one term per valid entry, so a position repeated among a row's
+ * valid entries would be counted twice.
+ *   topk_idx   [n_seq][T][K] int32, as for mla_sparse_decode_tokens (T = 1:
+ *              mla_sparse_decode's [B][K])
+ *   end_pos    [n_seq] int32
+ *   dev_status device int32 (required): MLA_DEV_DUPLICATE_INDEX is OR-ed in
+ *              when some row r = b*T + s holds a position t twice with
+ *              0 <= t <= end_pos[b] - T + s (the positions the row sees);
+ *              padding (entries < 0 or beyond that) is never flagged,
+ *              repeated or not.  A sequence whose end_pos is < T or > S_cap
+ *              is skipped and flagged MLA_DEV_BAD_END_POS, as the decode
+ *              would skip it.
+ * One kernel, one block per row, a bitmap of S_cap bits in shared memory.
+ * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (n_seq or T < 1,
+ * n_seq*T > 4096, K < 1 or > 1<<20, S_cap < 1 or > MLA_CHECK_MAX_S_CAP). */
+#define MLA_CHECK_MAX_S_CAP (1 << 20)
+int mla_check_selection(const int32_t *topk_idx, int K, const int32_t *end_pos, int n_seq, int T, int S_cap,
+                        int32_t *dev_status, mla_stream_t stream);
 
 /* mla_cache_append -- write T new tokens per sequence into the caches ("Query
  * heads" page, excerpt mla-init: the joint down-projection wkv_a emits the

@@ -111,16 +111,17 @@ extern "C" const char *mla_status_string(int code) {
         case MLA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
         default: break;
     }
-    if (code > 0 && code < 16) {
+    if (code > 0 && code < 32) {
         // one description per combination of the MLA_DEV_* bits
-        static const char *bit_names[4] = {"bad end_pos", "position outside rotary table",
-                                           "on-chip wait timed out", "partial score outside the exchange range"};
-        static char names[16][160];
+        static const char *bit_names[5] = {"bad end_pos", "position outside rotary table", "on-chip wait timed out",
+                                           "partial score outside the exchange range",
+                                           "repeated position in a selection row"};
+        static char names[32][208];
         static std::once_flag once;
         std::call_once(once, [] {
-            for (int c = 1; c < 16; ++c) {
+            for (int c = 1; c < 32; ++c) {
                 names[c][0] = 0;
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 5; ++i) {
                     if (!(c & (1 << i))) continue;
                     if (names[c][0]) strcat(names[c], "; ");
                     strcat(names[c], bit_names[i]);

@@ -23,6 +23,8 @@ MLA_DEV_BAD_END_POS = 1
 MLA_DEV_BAD_POSITION = 2
 MLA_DEV_TIMEOUT = 4
 MLA_DEV_SCORE_RANGE = 8
+MLA_DEV_DUPLICATE_INDEX = 16
+CHECK_MAX_S_CAP = 1 << 20
 
 
 class MLAError(RuntimeError):
@@ -63,6 +65,7 @@ def _load():
         "mla_linear_workspace_size": (Z, [I, I, I]),
         "mla_linear_bf16": (I, [P, P, I, I, I, P, P, P, Z, P, P]),
         "mla_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+        "mla_check_selection": (I, [P, I, P, I, I, I, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -77,7 +80,7 @@ EXPORTED = ("mla_rope_params_default", "mla_softmax_scale", "rope_freqs_init", "
             "mla_absorb_q", "mla_sparse_decode_workspace_size", "mla_sparse_decode", "mla_out_up",
             "mla_status_string", "mla_profile_hook", "mla_sparse_decode_static_ws", "mla_weight_dequant_fp8",
             "mla_cache_append", "mla_absorb_q_tokens", "mla_sparse_decode_tokens",
-            "mla_linear_workspace_size", "mla_linear_bf16", "mla_set_wait_limit_ns")
+            "mla_linear_workspace_size", "mla_linear_bf16", "mla_set_wait_limit_ns", "mla_check_selection")
 STATIC_WS_BYTES = 32 << 20
 
 
@@ -365,6 +368,26 @@ def mla_out_up(o_lat, wkv_b, out=None) -> torch.Tensor:
     _need(out, "out", torch.float32, (B, N_HEADS, D_V))
     _check(_lib.mla_out_up(_ptr(o_lat), _ptr(wkv_b), B, _ptr(out), _stream(o_lat.device)), "mla_out_up")
     return out
+
+
+def mla_check_selection(topk_idx, end_pos, S_cap: int, dev_status=None) -> torch.Tensor:
+    """Flags a position repeated among the valid entries of a selection row
+    (MLA_DEV_DUPLICATE_INDEX in the returned int32 status word; read it after
+    synchronising).  topk_idx [B, K] (one token per sequence) or [n, T, K];
+    end_pos [B] or [n]; S_cap is the cache capacity the selection indexes."""
+    if topk_idx.dim() == 2:
+        n, K = topk_idx.shape
+        T = 1
+    else:
+        n, T, K = topk_idx.shape
+    _need(topk_idx, "topk_idx", torch.int32)
+    _need(end_pos, "end_pos", torch.int32, (n,))
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=topk_idx.device)
+    _need(dev_status, "dev_status", torch.int32, (1,))
+    _check(_lib.mla_check_selection(_ptr(topk_idx), K, _ptr(end_pos), n, T, int(S_cap), _ptr(dev_status),
+                                    _stream(topk_idx.device)), "mla_check_selection")
+    return dev_status
 
 
 class ProfileHook:

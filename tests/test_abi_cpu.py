@@ -91,6 +91,14 @@ def test_host_argument_checks_return_codes_without_launching():
     bad = mla.rope_params()
     bad.rope_factor = 0.0
     assert lib.rope_freqs_init(GOOD, ctypes.byref(bad), nul) == -3
+    # the selection check: status word required, sizes, alignment
+    assert lib.mla_check_selection(GOOD, 8, GOOD, 1, 1, 16, nul, nul) == -1
+    assert lib.mla_check_selection(nul, 8, GOOD, 1, 1, 16, GOOD, nul) == -1
+    assert lib.mla_check_selection(MISALIGNED, 8, GOOD, 1, 1, 16, GOOD, nul) == -2
+    assert lib.mla_check_selection(GOOD, 8, GOOD, 1, 1, (1 << 20) + 1, GOOD, nul) == -3
+    assert lib.mla_check_selection(GOOD, 8, GOOD, 2049, 2, 16, GOOD, nul) == -3
+    assert lib.mla_check_selection(GOOD, 0, GOOD, 1, 1, 16, GOOD, nul) == -3
+    assert lib.mla_check_selection(GOOD, 8, GOOD, 1, 0, 16, GOOD, nul) == -3
     # workspace too small
     need = lib.mla_sparse_decode_workspace_size(2, 64)
     assert lib.mla_sparse_decode(GOOD, GOOD, GOOD, 16, GOOD, 64, GOOD, 2, 1.0, nul, GOOD, GOOD, need - 1, nul,
@@ -104,15 +112,17 @@ def test_status_strings():
     assert "end_pos" in mla.status_string(1)
     assert "timed out" in mla.status_string(4)
     assert "exchange range" in mla.status_string(8)
+    assert "repeated position" in mla.status_string(16)
     # every combination of device bits names each of its bits
-    for code in range(1, 16):
+    for code in range(1, 32):
         s = mla.status_string(code)
         assert ("end_pos" in s) == bool(code & 1)
         assert ("rotary table" in s) == bool(code & 2)
         assert ("timed out" in s) == bool(code & 4)
         assert ("exchange range" in s) == bool(code & 8)
+        assert ("repeated position" in s) == bool(code & 16)
     assert mla.status_string(-99) == "unknown status code"
-    assert mla.status_string(16) == "unknown status code"
+    assert mla.status_string(32) == "unknown status code"
 
 
 def test_python_wrappers_reject_cpu_tensors():

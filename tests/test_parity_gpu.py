@@ -313,6 +313,73 @@ def test_selection_order_does_not_matter():
     U.assert_attn_close(b.cpu().numpy(), a.cpu().numpy().astype(np.float64), "permuted selection")
 
 
+def _expected_dup(topk, end_pos, T):
+    """Plain set logic: does some row repeat a position it can see?"""
+    n = end_pos.shape[0]
+    rows = topk.reshape(n * T, -1)
+    for r in range(n * T):
+        b, s = divmod(r, T)
+        ep = int(end_pos[b])
+        e = ep - T + s + 1
+        if ep < T:
+            continue
+        valid = [int(t) for t in rows[r] if 0 <= int(t) < e]
+        if len(valid) != len(set(valid)):
+            return True
+    return False
+
+
+def test_check_selection_flags_repeated_visible_positions_only():
+    S = 100
+
+    def run(topk, end_pos, T=1):
+        tk = torch.tensor(topk, dtype=torch.int32).cuda()
+        ep = torch.tensor(end_pos, dtype=torch.int32).cuda()
+        st = mla.mla_check_selection(tk, ep, S)
+        torch.cuda.synchronize()
+        return int(st.item())
+
+    # distinct positions; padding (negative, at or beyond end_pos) repeated freely
+    assert run([[0, 5, 99, -1, -1, 7], [3, 49, 50, 50, 60, -7]], [100, 50]) == 0
+    # a repeated position that the row sees
+    assert run([[0, 5, 99, -1, -1, 7], [3, 49, 3, 50, 60, -7]], [100, 50]) == mla.MLA_DEV_DUPLICATE_INDEX
+    # at the edge of the visible range: end_pos - 1 repeated is flagged, end_pos repeated is not
+    assert run([[9, 9, 0]], [10]) == mla.MLA_DEV_DUPLICATE_INDEX
+    assert run([[10, 10, 0]], [10]) == 0
+    # multi-token: token 0 of a two-token sequence does not see position end_pos - 1, token 1 does
+    tk = [[[39, 39, 1], [2, 3, 4]]]
+    assert run(tk, [40], T=2) == 0
+    tk = [[[2, 3, 4], [39, 39, 1]]]
+    assert run(tk, [40], T=2) == mla.MLA_DEV_DUPLICATE_INDEX
+    # a sequence with a bad end_pos is skipped and reported as the decode reports it
+    assert run([[1, 1, 2], [4, 5, 6]], [0, 100]) == mla.MLA_DEV_BAD_END_POS
+    # random rows against plain set logic (rows of up to 2048 entries, a third of them repeating a position)
+    g = np.random.default_rng(11)
+    for trial in range(40):
+        n, T, K = int(g.integers(1, 5)), int(g.integers(1, 3)), int(g.choice([3, 64, 2048]))
+        end_pos = g.integers(T, S + 1, size=n)
+        topk = np.empty((n, T, K), dtype=np.int64)
+        for b in range(n):
+            for t in range(T):
+                row = g.permutation(np.arange(-5, S + 5))[:K] if K <= S + 10 else g.integers(-5, S + 5, size=K)
+                if K <= S + 10 and g.random() < 0.33:
+                    row[int(g.integers(0, K))] = row[int(g.integers(0, K))]
+                topk[b, t] = row
+        got = run(topk.tolist(), end_pos.tolist(), T=T)
+        want = mla.MLA_DEV_DUPLICATE_INDEX if _expected_dup(topk, end_pos, T) else 0
+        assert got == want, (trial, n, T, K)
+
+
+def test_check_selection_at_the_largest_cache():
+    # the bitmap spans the whole visible range of the largest cache the check accepts
+    S = mla.CHECK_MAX_S_CAP
+    tk = torch.tensor([[S - 1, 0, S // 2, S - 1]], dtype=torch.int32).cuda()
+    ep = torch.tensor([S], dtype=torch.int32).cuda()
+    assert int(mla.mla_check_selection(tk, ep, S).item()) == mla.MLA_DEV_DUPLICATE_INDEX
+    tk[0, 3] = S - 2
+    assert int(mla.mla_check_selection(tk, ep, S).item()) == 0
+
+
 def test_single_key_and_bad_end_pos_status():
     B, S = 3, 64
     t = synth.make_inputs(synth.small_workload(B, [64, 64, 64], k=1, K=1, S_cap=S), seed=9)
