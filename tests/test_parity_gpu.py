@@ -737,6 +737,15 @@ def test_host_buffer_step_matches_oracle_eager_and_captured():
     g()
     torch.cuda.synchronize()
     assert torch.equal(g.out, eager)
+    # the same inputs in one packed pinned buffer, copied in at once: the same bits
+    packed = torch.zeros(mla.HostDecodeStep.packed_bytes(B, K), dtype=torch.uint8).pin_memory()
+    for view, name in zip(mla.HostDecodeStep.packed_inputs(packed, B, K), ("q_nope", "q_pe", "topk_idx", "end_pos")):
+        view.copy_(h[name])
+    hs2 = mla.HostDecodeStep(B, K)
+    got = hs2.run_packed(packed, d["kv_cache"], d["pe_cache"], d["wkv_b"])
+    torch.cuda.synchronize()
+    hs2.check_status()
+    assert torch.equal(got, eager)
 
 
 def test_host_pipeline_steps_each_match_their_inputs():
