@@ -777,20 +777,21 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
     grid_dep_wait();   // the partials come from the preceding attention grid
     const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x * 4, half = c >= 256 ? 1 : 0;
     float M = -INFINITY;
+#pragma unroll 8
     for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_lse[(((size_t)b * n_split + s) * 2 + half) * H + h]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < n_split; ++s) {
-            const size_t u = (size_t)b * n_split + s;
-            const float lse = part_lse[(u * 2 + half) * H + h];
-            if (lse == -INFINITY) continue;
-            const float w = exp2f(lse - M);
-            L += w;
-            const float4 v = *reinterpret_cast<const float4 *>(part_o + (u * H + h) * C + c);
-            acc.x = fmaf(w, v.x, acc.x), acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z), acc.w = fmaf(w, v.w, acc.w);
-        }
+    // an empty split has weight 0 and a zero o (its unit writes zeros): every split is
+    // loaded unconditionally, so that the loads of several splits are in flight at once
+#pragma unroll 8
+    for (int s = 0; s < n_split; ++s) {
+        const size_t u = (size_t)b * n_split + s;
+        const float lse = part_lse[(u * 2 + half) * H + h];
+        const float w = (M == -INFINITY || lse == -INFINITY) ? 0.f : exp2f(lse - M);
+        L += w;
+        const float4 v = *reinterpret_cast<const float4 *>(part_o + (u * H + h) * C + c);
+        acc.x = fmaf(w, v.x, acc.x), acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z), acc.w = fmaf(w, v.w, acc.w);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const size_t o = ((size_t)b * H + h) * C + c;

@@ -28,6 +28,7 @@ constexpr int NMAX = 64;                       // sequences per pass
 constexpr int A_BOX = 128 * 128;               // [128 d][64 c] box of W_UV, bytes
 constexpr int B_ATOM = NMAX * 128;             // [64 b][64 c] atom column of the o tile, bytes
 constexpr int SMEM_BYTES = 8 * A_BOX + 8 * B_ATOM + 1024;
+constexpr int MERGE_ROWS = 2, MERGE_SPLITS = 128;   // split partials merged here: rows and splits per row, at most
 struct Bars {
     uint64_t a_full, b_full, mma_done, drain;
     uint32_t tmem_base;
@@ -64,39 +65,69 @@ __device__ __forceinline__ void stage_f32(const float *__restrict__ o_lat, int h
     }
 }
 
-// Split partials of one pass -> bf16 operand tile: each query row's latent
-// output o is merged from its n_split partials (normalised o of every split,
-// and the log2 of each split's softmax mass, one per latent half and head)
-// exactly as the split-combine kernel does, then rounded to bf16.
+// Split partials -> bf16 operand tile, for the one or two query rows of a
+// split selection: each row's latent output o is merged from its n_split
+// partials (normalised o of every split, and the log2 of each split's softmax
+// mass, one per latent half and head), o = sum_s 2^(lse_s - M) o_s / sum_s
+// 2^(lse_s - M) with M the largest lse_s, as the split-combine kernel merges
+// them.  One warp per (row, half) turns the masses into normalised weights in
+// shared memory; then each thread sums one 16-byte chunk of a row over the
+// splits, with the loads of several splits in flight at once.
 __device__ __forceinline__ void stage_partials(const float *__restrict__ part_o, const float *__restrict__ part_lse,
-                                               int n_split, int h, int n0, int nb, int N, uint8_t *sB, int tid) {
-    const int total = N * 64;
-    for (int u = tid; u < total; u += 128) {
-        const int row = u >> 6, ch = u & 63, half = ch >= 32 ? 1 : 0;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+                                               int n_split, int h, int n0, int nb, int N, uint8_t *sB, int tid,
+                                               float (*wts)[2][MERGE_SPLITS]) {
+    const int warp = tid >> 5, lane = tid & 31;
+    {
+        const int row = warp >> 1, half = warp & 1;   // four warps: rows 0..1, halves 0..1
         if (row < nb) {
+            // each lane holds the masses of splits lane, lane+32, ... (one load each)
+            constexpr int PER_LANE = MERGE_SPLITS / 32;
             const size_t u0 = (size_t)(n0 + row) * n_split;
+            float lse[PER_LANE];
             float M = -INFINITY;
-            for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, part_lse[((u0 + sp) * 2 + half) * H + h]);
-            float L = 0.f;
-            if (M != -INFINITY) {
-                for (int sp = 0; sp < n_split; ++sp) {
-                    const float lse = part_lse[((u0 + sp) * 2 + half) * H + h];
-                    if (lse == -INFINITY) continue;
-                    const float w = exp2f(lse - M);
-                    L += w;
-                    const float4 *src = reinterpret_cast<const float4 *>(part_o + ((u0 + sp) * H + h) * C + ch * 8);
-                    const float4 v0 = src[0], v1 = src[1];
-                    a.x = fmaf(w, v0.x, a.x), a.y = fmaf(w, v0.y, a.y), a.z = fmaf(w, v0.z, a.z), a.w = fmaf(w, v0.w, a.w);
-                    c.x = fmaf(w, v1.x, c.x), c.y = fmaf(w, v1.y, c.y), c.z = fmaf(w, v1.z, c.z), c.w = fmaf(w, v1.w, c.w);
-                }
+#pragma unroll
+            for (int k = 0; k < PER_LANE; ++k) {
+                const int sp = lane + 32 * k;
+                lse[k] = sp < n_split ? part_lse[((u0 + sp) * 2 + half) * H + h] : -INFINITY;
+                M = fmaxf(M, lse[k]);
             }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            float L = 0.f;
+#pragma unroll
+            for (int k = 0; k < PER_LANE; ++k) {
+                lse[k] = (M == -INFINITY || lse[k] == -INFINITY) ? 0.f : exp2f(lse[k] - M);   // now the weight
+                L += lse[k];
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            a.x *= inv, a.y *= inv, a.z *= inv, a.w *= inv;
-            c.x *= inv, c.y *= inv, c.z *= inv, c.w *= inv;
+#pragma unroll
+            for (int k = 0; k < PER_LANE; ++k)
+                if (lane + 32 * k < n_split) wts[row][half][lane + 32 * k] = lse[k] * inv;
         }
-        *reinterpret_cast<uint4 *>(sB + (ch >> 3) * B_ATOM + sw128(row, ch & 7)) =
-            make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(c.x, c.y), pack_bf16(c.z, c.w));
+    }
+    __syncthreads();
+    // 16-byte chunk q (4 floats) of row `row`: 128 per row, 8 bytes of the bf16 tile
+    for (int u = tid; u < N * 128; u += 128) {
+        const int row = u >> 7, q = u & 127, half = q >= 64 ? 1 : 0;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row < nb) {
+            const float *w = wts[row][half];
+            const float4 *src = reinterpret_cast<const float4 *>(part_o + ((size_t)(n0 + row) * n_split * H + h) * C) + q;
+            constexpr size_t STEP = (size_t)H * C / 4;   // float4s between two splits of the row
+#pragma unroll 16
+            for (int sp = 0; sp < n_split; ++sp) {
+                // an empty split has weight 0 and a zero o (its unit writes zeros), so
+                // every split is loaded unconditionally and the loads go out together
+                const float ws = w[sp];
+                const float4 v = src[sp * STEP];
+                a.x = fmaf(ws, v.x, a.x), a.y = fmaf(ws, v.y, a.y), a.z = fmaf(ws, v.z, a.z), a.w = fmaf(ws, v.w, a.w);
+            }
+        }
+        const int ch = q >> 1;   // the 16-byte bf16 chunk (8 latent columns) this half-chunk belongs to
+        *reinterpret_cast<uint2 *>(sB + (ch >> 3) * B_ATOM + sw128(row, ch & 7) + (q & 1) * 8) =
+            make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
     }
 }
 
@@ -151,7 +182,8 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
                 b_issued = pass + 1;
             }
         } else if (part_o) {
-            stage_partials(part_o, part_lse, n_split, h, n0, nb, N, sB, tid);
+            __shared__ float wts[MERGE_ROWS][2][MERGE_SPLITS];
+            stage_partials(part_o, part_lse, n_split, h, n0, nb, N, sB, tid, wts);
             fence_proxy_async_smem();
         } else {
             stage_f32(o_f32, h, n0, nb, N, sB, tid);
@@ -237,6 +269,8 @@ int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv
     } else {
         omap = wmap;   // unused
     }
+    // split partials are merged here only for the one or two rows of a split selection
+    if (part_o && (B > outup::MERGE_ROWS || n_split < 1 || n_split > outup::MERGE_SPLITS)) return MLA_ERR_SIZE;
     static std::atomic<bool> smem_set[64];
     if (!smem_attr_once(smem_set, outup::out_up_kernel, outup::SMEM_BYTES)) return MLA_ERR_CUDA;
     const cudaError_t err = launch_k(pdl, outup::out_up_kernel, dim3(H), dim3(128), outup::SMEM_BYTES, s, wmap,
