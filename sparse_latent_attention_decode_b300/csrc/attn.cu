@@ -329,10 +329,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
     tc_fence_after();
     // the block count is read where it is used (from shared memory) rather than
     // held in a register across the whole kernel
-    // The dependent grid (value up-projection) may start its prologue now; it
-    // reads this grid's output only after its own griddepcontrol.wait, which
-    // returns once this grid -- and so the grid before it -- has completed.
-    if (tid == 0) grid_dep_launch();
     const uint32_t tmem = bars.tmem_base;
     const Deadline deadline = make_deadline(p.wait_ns);
 
@@ -430,6 +426,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                     mma_commit(&bars.empty[s]);
                 }
             }
+            // The dependent grid (value up-projection or split combine) may be
+            // scheduled once every CTA has issued its last QK: all of this CTA's
+            // cache reads have landed by then, so the up-projection's weight loads
+            // do not compete with the gather and the Q loads at the start (a CTA
+            // with no blocks counts when it exits).  The dependent reads this
+            // grid's output only after its own griddepcontrol.wait, which returns
+            // once this grid -- and so the grid before it -- has completed.
+            if (warp == QK_WARP) grid_dep_launch();
             if (!ok) fail(p);
             // drain: every MMA this thread issued has completed before TMEM is released
             mma_commit(&bars.drain[warp - QK_WARP]);
