@@ -137,6 +137,8 @@ struct Params {
     float *o_out;       // n_split == 1: normalised o, fp32 [B][128][512] (or NULL)
     uint16_t *o_b16;    // n_split == 1: normalised o, bf16 [B][128][512] (or NULL)
     float *part_o;      // n_split > 1: per-split normalised o, fp32 [B*n_split][128][512]
+    uint16_t *part_o16; // n_split > 1 instead of part_o, when the up-projection merges the splits:
+                        // the same partials as bf16 (its operand is bf16 anyway)
     float *part_lse;    // n_split > 1: log2 of the split's softmax mass, [B*n_split][2][128]
     int32_t *status;
     uint64_t wait_ns;   // limit of every bounded wait
@@ -699,7 +701,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         const bool tload = ok && unit_blocks(bars) > 0;   // warp-uniform: tcgen05.ld is warp-collective
         const bool have = tload && lt > 0.f;
         const float inv = have ? 1.f / lt : 0.f;
-        const bool bf16_out = p.n_split == 1 && p.o_b16;
+        const bool part16 = p.n_split > 1 && p.part_o16;
+        const bool bf16_out = (p.n_split == 1 && p.o_b16) || part16;
         const int cw0 = ocol(w), ncol = ocol(w + 1) - cw0;
         const int esz = bf16_out ? 2 : 4;
         const int nch = ncol * esz / 16;                 // 16-byte chunks of this warpgroup's part of a row
@@ -742,9 +745,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         asm volatile("bar.sync %0, %1;" ::"r"(1 + w), "r"(WG_THREADS) : "memory");
         {
             const int col0 = 256 * r + cw0;
-            const size_t row0 = bf16_out || p.n_split == 1 ? (size_t)b * H : (size_t)unit * H;
-            uint8_t *dst = bf16_out ? reinterpret_cast<uint8_t *>(p.o_b16 + row0 * C + col0)
-                                    : reinterpret_cast<uint8_t *>((p.n_split == 1 ? p.o_out : p.part_o) + row0 * C + col0);
+            const size_t row0 = p.n_split == 1 ? (size_t)b * H : (size_t)unit * H;
+            uint8_t *dst = part16     ? reinterpret_cast<uint8_t *>(p.part_o16 + row0 * C + col0)
+                           : bf16_out ? reinterpret_cast<uint8_t *>(p.o_b16 + row0 * C + col0)
+                                      : reinterpret_cast<uint8_t *>((p.n_split == 1 ? p.o_out : p.part_o) + row0 * C + col0);
             const size_t pitch = bf16_out ? C * 2 : C * 4;   // bytes between the rows of two heads
 #pragma unroll 4
             for (int idx = wtid; idx < H * nch; idx += WG_THREADS) {
@@ -871,9 +875,14 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
         p.o_out = o_out;
         p.o_b16 = o_b16;
     } else {
+        // the partials of a split the up-projection merges are written as bf16
+        // (half the bytes each way); the combine kernel reads fp32 ones
         const size_t units = (size_t)B * n_split;
-        p.part_o = static_cast<float *>(ws);
-        p.part_lse = p.part_o + units * H * C;
+        if (merge_later)
+            p.part_o16 = static_cast<uint16_t *>(ws);
+        else
+            p.part_o = static_cast<float *>(ws);
+        p.part_lse = static_cast<float *>(ws) + units * H * C;
     }
     static std::atomic<bool> smem_set[64];
     static std::atomic<bool> smem_set16[64];

@@ -85,8 +85,8 @@ extern "C" int mla_sparse_decode_tokens(const mla_bf16 *q_lat, const mla_bf16 *k
         int n_split = 1;
         attn_partials(B, K, S_cap, ws + L.attn, &part_o, &part_lse, &n_split);
         if (merge_in_up && n_split > 1)
-            return launch_out_up(nullptr, nullptr, wkv_b, B, out_f32, out_b16, dev_status, s, pdl, part_o, part_lse,
-                                 n_split);
+            return launch_out_up(nullptr, nullptr, wkv_b, B, out_f32, out_b16, dev_status, s, pdl,
+                                 reinterpret_cast<const uint16_t *>(part_o), part_lse, n_split);
         return launch_out_up(nullptr, o_b16, wkv_b, B, out_f32, out_b16, dev_status, s, pdl);
     }
     return MLA_OK;

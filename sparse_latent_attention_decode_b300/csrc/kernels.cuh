@@ -14,9 +14,10 @@ namespace mla {
 // attention path); exactly one of them is non-NULL.  The head outputs go to
 // out (fp32) or, when out_b16 is non-NULL, to out_b16 (bf16).
 // With part_o non-NULL (and o_f32, o_b16 NULL) the operand is merged from
-// the attention kernel's split partials (part_o, part_lse, n_split per row).
+// the attention kernel's split partials (part_o as bf16, written so by a
+// launch_attn with merge_later; part_lse; n_split per row).
 int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
-                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl, const float *part_o = nullptr,
+                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl, const uint16_t *part_o = nullptr,
                   const float *part_lse = nullptr, int n_split = 0);
 
 // Sparse attention (tensor-core kernel + split combine) over B query rows,
@@ -36,7 +37,8 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
                 const int32_t *end_pos, int B, int T, float softmax_scale, float *o_out, uint16_t *o_b16, void *ws,
                 int32_t *status, cudaStream_t s, int *launches, bool merge_later = false);
 // Where the split partials of launch_attn(B, K, S_cap) live in its workspace
-// (part_o [B*n_split][128][512], part_lse [B*n_split][2][128]); n_split 1: none.
+// (part_o [B*n_split][128][512], fp32 -- bf16 when launched with merge_later --
+// and part_lse [B*n_split][2][128]); n_split 1: none.
 void attn_partials(int B, int K, int S_cap, void *ws, float **part_o, float **part_lse, int *n_split);
 
 // Launch `kern` on stream s.  With pdl set, the launch allows programmatic

@@ -67,13 +67,14 @@ __device__ __forceinline__ void stage_f32(const float *__restrict__ o_lat, int h
 
 // Split partials -> bf16 operand tile, for the one or two query rows of a
 // split selection: each row's latent output o is merged from its n_split
-// partials (normalised o of every split, and the log2 of each split's softmax
-// mass, one per latent half and head), o = sum_s 2^(lse_s - M) o_s / sum_s
-// 2^(lse_s - M) with M the largest lse_s, as the split-combine kernel merges
-// them.  One warp per (row, half) turns the masses into normalised weights in
-// shared memory; then each thread sums one 16-byte chunk of a row over the
-// splits, with the loads of several splits in flight at once.
-__device__ __forceinline__ void stage_partials(const float *__restrict__ part_o, const float *__restrict__ part_lse,
+// partials (normalised o of every split as bf16, and the log2 of each split's
+// softmax mass, one per latent half and head), o = sum_s 2^(lse_s - M) o_s /
+// sum_s 2^(lse_s - M) with M the largest lse_s, as the split-combine kernel
+// merges them (in fp32).  One warp per (row, half) turns the masses into
+// normalised weights in shared memory; then each thread sums four latent
+// columns of a row over the splits, with the loads of several splits in
+// flight at once.
+__device__ __forceinline__ void stage_partials(const uint16_t *__restrict__ part_o, const float *__restrict__ part_lse,
                                                int n_split, int h, int n0, int nb, int N, uint8_t *sB, int tid,
                                                float (*wts)[2][MERGE_SPLITS]) {
     const int warp = tid >> 5, lane = tid & 31;
@@ -108,21 +109,22 @@ __device__ __forceinline__ void stage_partials(const float *__restrict__ part_o,
         }
     }
     __syncthreads();
-    // 16-byte chunk q (4 floats) of row `row`: 128 per row, 8 bytes of the bf16 tile
+    // piece q (4 latent columns) of row `row`: 128 per row, 8 bytes of partial and of the bf16 tile
     for (int u = tid; u < N * 128; u += 128) {
         const int row = u >> 7, q = u & 127, half = q >= 64 ? 1 : 0;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row < nb) {
             const float *w = wts[row][half];
-            const float4 *src = reinterpret_cast<const float4 *>(part_o + ((size_t)(n0 + row) * n_split * H + h) * C) + q;
-            constexpr size_t STEP = (size_t)H * C / 4;   // float4s between two splits of the row
+            const uint2 *src = reinterpret_cast<const uint2 *>(part_o + ((size_t)(n0 + row) * n_split * H + h) * C) + q;
+            constexpr size_t STEP = (size_t)H * C / 4;   // 4-element pieces between two splits of the row
 #pragma unroll 16
             for (int sp = 0; sp < n_split; ++sp) {
                 // an empty split has weight 0 and a zero o (its unit writes zeros), so
                 // every split is loaded unconditionally and the loads go out together
                 const float ws = w[sp];
-                const float4 v = src[sp * STEP];
-                a.x = fmaf(ws, v.x, a.x), a.y = fmaf(ws, v.y, a.y), a.z = fmaf(ws, v.z, a.z), a.w = fmaf(ws, v.w, a.w);
+                const uint2 v = src[sp * STEP];
+                a.x = fmaf(ws, bflo(v.x), a.x), a.y = fmaf(ws, bfhi(v.x), a.y);
+                a.z = fmaf(ws, bflo(v.y), a.z), a.w = fmaf(ws, bfhi(v.y), a.w);
             }
         }
         const int ch = q >> 1;   // the 16-byte bf16 chunk (8 latent columns) this half-chunk belongs to
@@ -134,7 +136,7 @@ __device__ __forceinline__ void stage_partials(const float *__restrict__ part_o,
 __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ CUtensorMap wmap,
                                                         const __grid_constant__ CUtensorMap omap,
                                                         const float *__restrict__ o_f32, bool o_is_b16, int B,
-                                                        const float *__restrict__ part_o,
+                                                        const uint16_t *__restrict__ part_o,
                                                         const float *__restrict__ part_lse, int n_split,
                                                         float *__restrict__ out, uint16_t *__restrict__ out_b16,
                                                         int32_t *status, uint64_t wait_ns) {
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
 }  // namespace outup
 
 int launch_out_up(const float *o_f32, const uint16_t *o_b16, const uint16_t *wkv_b, int B, float *out,
-                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl, const float *part_o,
+                  uint16_t *out_b16, int32_t *status, cudaStream_t s, bool pdl, const uint16_t *part_o,
                   const float *part_lse, int n_split) {
     CUtensorMap wmap, omap;
     {
