@@ -100,6 +100,9 @@ constexpr int IDX_CAP16 = IDX_BYTES / 2;     // entries as 16-bit positions (cac
 constexpr int QROPE = H * 64;                // rotary part of Q_r: 128 heads x 32 bf16 (64B swizzle)
 constexpr int SEND = RECV;                   // this CTA's partial scores of one block, shipped by bulk copy
 constexpr int QUARTER = RECV / 4;            // one warp's 32 rows of a block's scores, its own bulk copy
+constexpr int Q_STAGE = 2;                   // Q_r's latent part arrives by TMA in gather stages 2 and 3
+constexpr int QBOX = 64 * H * 2;             // one 128B-swizzled box of Q_r: 64 latent columns x 128 heads
+static_assert((NS - Q_STAGE) * STAGE >= 4 * QBOX && (Q_STAGE * STAGE) % 1024 == 0, "Q_r staging in the gather stages");
 constexpr int SMEM_BYTES = NS * STAGE + NRECV * RECV + QROPE + IDX_BYTES + SEND + 1024;
 constexpr uint32_t O_COL = 0, Q_COL = 256, S_COL = 384, TMEM_COLS = 512;   // S buffer k at S_COL + 64 k
 constexpr int THREADS = 640;                 // 20 warps
@@ -151,6 +154,7 @@ struct Bars {
     // its barrier in order, and a parity wait can never refer to a phase two
     // behind or ahead.  s_free is waited by the QK issuer alone, in order.
     uint64_t s_full[NWG], pv_done[NWG], s_free[2], q_ready;
+    uint64_t q_full;       // Q_r has landed (TMA): latent part in stages 2-3, rotary part in place
     uint64_t p_full[NWG];  // P of warpgroup w's blocks (one barrier per warpgroup: with three, the
                            // warpgroups of blocks j and j+2 differ and must not share a phase)
     uint64_t recv_full[NRECV][4];   // quarter q (heads 32q .. 32q+31) of the peer's block in slot k
@@ -230,7 +234,8 @@ __device__ __forceinline__ void add_f16x2(uint32_t w, float &lo_acc, float &hi_a
 
 
 template <bool IDX16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_kernel(Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap qrmap, Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Bars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -305,6 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             mbar_init(&bars.m_ready[k], WG_THREADS);
         }
         mbar_init(&bars.q_ready, NWG * WG_THREADS);
+        mbar_init(&bars.q_full, 1);
         mbar_init(&bars.l_ready, NWG * WG_THREADS);
         mbar_init(&bars.drain[0], 1);
         mbar_init(&bars.drain[1], 1);
@@ -368,6 +374,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
                 fail(p);
                 break;
             }
+            // stages 2 and 3 first hold Q_r's latent part: their first blocks wait
+            // until the softmax warpgroups have moved it into TMEM
+            if (j >= Q_STAGE && j < NS && !warp_wait(&bars.q_ready, 0, deadline)) {
+                fail(p);
+                break;
+            }
             const uint32_t base = smem_u32(stages + s * STAGE);
             const int bofs = j * NK;
 #pragma unroll
@@ -388,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
             bool ok = true;
             if (warp == QK_WARP) {
                 constexpr uint32_t idesc_qk = idesc_bf16(128, NK, false, false);
-                ok = wait_until(&bars.q_ready, 0, deadline);
+                ok = wait_until(&bars.q_ready, 0, deadline) && wait_until(&bars.q_full, 0, deadline);
                 const uint32_t qr = smem_u32(qrope);
                 for (int j = 0; ok && j < unit_blocks(bars); ++j) {
                     const int s = j % NS, k = j & 1;
@@ -465,38 +477,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1) attn_ker
         // the buffers the epilogue writes: both wait for it to complete
         grid_dep_wait();
         if (unit_blocks(bars) > 0) {
-            // Q_r: latent [256r, 256r+256) -> TMEM as 128 bf16 pairs (warpgroup w
-            // stores 16-column groups 8w/NWG .. 8(w+1)/NWG - 1); rotary [32r, 32r+32)
-            // -> shared memory, K-major with the 64-byte swizzle (warpgroup 1)
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + h) * QL);
-            // every load of the row is issued before the first store, so their latencies overlap
-            constexpr int QMAX = (8 + NWG - 1) / NWG;   // 16-column groups of a warpgroup, at most
-            const int g0 = (8 * w) / NWG, ng = (8 * (w + 1)) / NWG - g0;
-            uint4 qv[QMAX][4], qr[4];
+            // Q_r by TMA: the latent part [256r, 256r+256) as four 128B-swizzled boxes
+            // of 64 columns x 128 heads into gather stages 2-3 (whose first blocks wait
+            // for q_ready), the rotary part [512+32r, 512+32r+32) straight into its
+            // place, K-major with the 64-byte swizzle.  Through the tensor memory
+            // accelerator its 72 KB do not occupy the load path that the gather's
+            // first cp.async wait for (per-thread loads of Q delayed the first block by
+            // about 3.5 us).
+            const uint32_t qst = smem_u32(stages + Q_STAGE * STAGE);
+            if (w == 0 && wtid == 0) {
+                mbar_expect_tx(&bars.q_full, 4 * QBOX + QROPE);
 #pragma unroll
-            for (int i = 0; i < QMAX; ++i)
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    qv[i][q] = i < ng ? qrow[(256 * r) / 8 + (g0 + i) * 4 + q] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) qr[c] = w == 1 ? qrow[(512 + 32 * r) / 8 + c] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int i = 0; i < QMAX; ++i) {
-                if (i >= ng) break;
-                uint32_t v[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    v[4 * q] = qv[i][q].x, v[4 * q + 1] = qv[i][q].y, v[4 * q + 2] = qv[i][q].z, v[4 * q + 3] = qv[i][q].w;
-                tmem_st16(trow + Q_COL + 16 * (g0 + i), v);
+                for (int k = 0; k < 4; ++k) tma_load_2d(qst + k * QBOX, &qmap, 256 * r + 64 * k, b * H, &bars.q_full);
+                tma_load_2d(smem_u32(qrope), &qrmap, C + 32 * r, b * H, &bars.q_full);
             }
-            if (w == 1) {
+            if (warp_wait(&bars.q_full, 0, deadline)) {
+                // latent Q_r -> TMEM as 128 bf16 pairs per head: warpgroup w stores the
+                // 16-column groups 8w/NWG .. 8(w+1)/NWG - 1 (group g = columns 32g ..
+                // 32g+31, chunks 4(g&1) .. 4(g&1)+3 of box g/2)
+                constexpr int QMAX = (8 + NWG - 1) / NWG;   // 16-column groups of a warpgroup, at most
+                const int g0 = (8 * w) / NWG, ng = (8 * (w + 1)) / NWG - g0;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4 *>(qrope + sw64(h, c)) = qr[c];
-                fence_proxy_async_smem();
+                for (int i = 0; i < QMAX; ++i) {
+                    if (i >= ng) break;
+                    const int g = g0 + i;
+                    const uint32_t box = qst + (g >> 1) * QBOX;
+                    uint32_t v[16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(v[4 * q]), "=r"(v[4 * q + 1]), "=r"(v[4 * q + 2]), "=r"(v[4 * q + 3])
+                                     : "r"(box + sw128(h, (g & 1) * 4 + q)));
+                    tmem_st16(trow + Q_COL + 16 * g, v);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars.q_ready);
+            } else {
+                ok = false;
+                // no copy may land in this CTA's shared memory after it has exited
+                if (w == 0 && wtid == 0) wait_until(&bars.q_full, 0, globaltimer_ns() + DRAIN_NS);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bars.q_ready);
         }
         const uint32_t recv_local = smem_u32(recv);
         const uint32_t recv_peer = map_peer(recv_local, peer);
@@ -884,6 +905,17 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
             p.part_o = static_cast<float *>(ws);
         p.part_lse = static_cast<float *>(ws) + units * H * C;
     }
+    // Q_r of a unit arrives by TMA: q_lat viewed as [B*128 rows][576], boxes of
+    // 64 latent columns (128B swizzle) and of the 32 rotary columns (64B swizzle)
+    CUtensorMap qmap, qrmap;
+    {
+        const uint64_t dims[2] = {(uint64_t)QL, (uint64_t)B * H};
+        const uint64_t strides[1] = {(uint64_t)QL * 2};
+        const uint32_t box[2] = {64, H}, rbox[2] = {32, H};
+        if (!make_tmap_bf16(&qmap, q_lat, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap_bf16(&qrmap, q_lat, 2, dims, strides, rbox, CU_TENSOR_MAP_SWIZZLE_64B))
+            return MLA_ERR_CUDA;
+    }
     static std::atomic<bool> smem_set[64];
     static std::atomic<bool> smem_set16[64];
     auto kern = idx16 ? attn::attn_kernel<true> : attn::attn_kernel<false>;
@@ -893,7 +925,7 @@ int launch_attn(const uint16_t *q_lat, const uint16_t *kv, const uint16_t *pe, i
     // With the timing events in the stream the kernels are launched plainly:
     // an event between two grids would separate them anyway.
     if (timed && cudaEventRecord(hook.start, s) != cudaSuccess) return MLA_ERR_CUDA;
-    if (launch_k(!timed, kern, dim3(2 * B * n_split), dim3(attn::THREADS), attn::SMEM_BYTES, s, p) !=
+    if (launch_k(!timed, kern, dim3(2 * B * n_split), dim3(attn::THREADS), attn::SMEM_BYTES, s, qmap, qrmap, p) !=
         cudaSuccess)
         return MLA_ERR_CUDA;
     if (timed && cudaEventRecord(hook.stop, s) != cudaSuccess) return MLA_ERR_CUDA;

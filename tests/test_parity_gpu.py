@@ -158,6 +158,9 @@ SMALL = [
     (3, [1000, 70, 3000], 2048, 2048, 3000, "uniform"),    # rows mostly padding: units cut short or left empty
     (40, [4096] * 40, 4096, 4096, 4096, "uniform"),        # one unit of 4096 entries (16-bit staged positions)
     (2, [70000, 65600], 3000, 3000, 70000, "uniform"),     # a cache of 70,000 rows: 32-bit staged positions
+    # few splits merged by the up-projection from bf16 partials (the largest share of their rounding)
+    (1, [150], 150, 150, 256, "all"),                       # three units, the last one ragged
+    (2, [128, 100], 128, 128, 256, "uniform"),              # two units per row, two rows
 ]
 
 
