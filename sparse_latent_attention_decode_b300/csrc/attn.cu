@@ -515,8 +515,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 mbar_arrive(&bars.q_ready);
             } else {
                 ok = false;
-                // no copy may land in this CTA's shared memory after it has exited
-                if (w == 0 && wtid == 0) wait_until(&bars.q_full, 0, globaltimer_ns() + DRAIN_NS);
+                // the copies of Q_r may still be landing: wait for them (for at most the drain
+                // limit) before warpgroup 1 stages its output in stages 2-3 or the CTA exits
+                warp_wait(&bars.q_full, 0, make_deadline(DRAIN_NS));
             }
         }
         const uint32_t recv_local = smem_u32(recv);
