@@ -40,7 +40,11 @@
 //   warp 11     forwards each completed PV(j) to the peer as a ring credit
 //               (warp 10 is idle);
 //   warps 12-15 softmax of the even blocks, warps 16-19 of the odd blocks
-//               (ping-pong): one thread per head, all 64 keys of its block.
+//               (ping-pong): one thread per head, all 64 keys of its block;
+//               before the first block, one of their threads loads Q_r by
+//               TMA (the latent part through gather stages 2-3, whose first
+//               blocks wait for it, the rotary part into its place) and the
+//               warpgroups move its latent part into TMEM.
 // The selection of the unit is staged in shared memory once (positions
 // outside [0, end_pos) become -1), so no global index load sits on the
 // per-block path: as 32-bit positions (up to 2048 entries per unit), or as
