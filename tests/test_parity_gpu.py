@@ -620,6 +620,30 @@ def test_multi_token_decode_matches_oracle(case):
     U.assert_attn_close(out.cpu().numpy().reshape(-1, 128, 128), ora.reshape(-1, 128, 128), "multi-token")
 
 
+def test_multi_token_decode_at_full_context_on_sampled_sequences():
+    # the multi-token row as bench.py times it: 32 sequences x 2 query tokens over a
+    # 16384-row cache, a top-2048 selection per token; compared with the oracle on
+    # sampled sequences (both tokens of each), the rest checked for finiteness
+    n, T, K = 32, 2, 2048
+    wl = synth.small_workload(n, [16384] * n, k=K, K=K, S_cap=16384)
+    t = synth.make_token_inputs(wl, T, seed=59, threads=16)
+    d = _dev(t)
+    cis = mla.rope_freqs_init()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_lat = mla.mla_absorb_q_tokens(d["q_nope"], d["q_pe"], cis, d["end_pos"], d["wkv_b"], dev_status=st)
+    out = mla.mla_sparse_decode_tokens(q_lat, d["kv_cache"], d["pe_cache"], d["topk_idx"], d["end_pos"], U.SCALE,
+                                       wkv_b=d["wkv_b"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.cpu()
+    assert torch.isfinite(got).all()
+    bs = [0, 17, 31]
+    x = {k: synth.to_f64(t[k][bs]) for k in ("q_nope", "q_pe", "kv_cache", "pe_cache", "topk_idx", "end_pos")}
+    ora = O.decode_tokens(x["q_nope"], x["q_pe"], x["kv_cache"], x["pe_cache"], synth.to_f64(t["wkv_b"]),
+                          x["topk_idx"], x["end_pos"], U.INV_FREQ, U.SCALE)
+    U.assert_attn_close(got[bs].numpy().reshape(-1, 128, 128), ora.reshape(-1, 128, 128), "multi-token, full context")
+
+
 def test_multi_token_one_token_equals_the_single_token_entry():
     B, K = 6, 512
     t = synth.make_inputs(synth.small_workload(B, [900, 512, 1000, 64, 777, 1], k=K, K=K, S_cap=1024), seed=53)
