@@ -597,6 +597,7 @@ TOKENS = [
     ([1000, 64, 777], 4, 256, 256),
     ([2048, 1500], 3, 1100, 1100),       # several splits per query row
     ([5, 9, 600, 4096] * 5, 2, 300, 320),  # 40 query rows, ragged K tail
+    ([1500], 2, 1100, 1100),             # two query rows of one sequence: splits merged in the up-projection
 ]
 
 
