@@ -163,3 +163,27 @@ def test_packed_host_inputs_are_disjoint_aligned_views():
         t.view(torch.uint8).fill_(i + 1)
     assert int((buf == 1).sum()) == q_nope.numel() * 2
     assert int((buf == 4).sum()) == end.numel() * 4
+
+
+@pytest.mark.parametrize("B,K", [(1, 1001), (3, 256), (64, 2048), (4096, 64)])
+def test_packed_host_inputs_layout(B, K):
+    # the host-buffer step copies its four inputs in as one buffer: each part at a
+    # 256-byte aligned offset, in order, not overlapping, with the shapes and
+    # dtypes of the separate inputs
+    import torch
+    n = mla.HostDecodeStep.packed_bytes(B, K)
+    buf = torch.zeros(n, dtype=torch.uint8)
+    parts = mla.HostDecodeStep.packed_inputs(buf, B, K)
+    want = [((B, 128, 128), torch.bfloat16), ((B, 128, 64), torch.bfloat16), ((B, K), torch.int32),
+            ((B,), torch.int32)]
+    base = buf.data_ptr()
+    end = 0
+    for v, (shape, dtype) in zip(parts, want):
+        assert tuple(v.shape) == shape and v.dtype == dtype and v.is_contiguous()
+        off = v.data_ptr() - base
+        assert off % 256 == 0 and off >= end
+        end = off + v.numel() * v.element_size()
+    assert end <= n < end + 256
+    # writing through one view leaves the others untouched
+    parts[2].fill_(-1)
+    assert int(parts[0].view(torch.int16).abs().sum()) == 0 and int(parts[3].sum()) == 0
