@@ -207,8 +207,8 @@ size_t mla_sparse_decode_workspace_size(int B, int K);
  * sets MLA_DEV_SCORE_RANGE, since the error of one exchanged copy can then
  * reach a whole unit of the raw score.  With wkv_b, o is rounded to bf16 as
  * the up-projection's operand; when the selection of one or two query rows
- * is split over several SM pairs, each split's normalised o is kept as bf16
- * until the up-projection merges the splits (in fp32).
+ * is split over several SM pairs, each split's normalised o is kept as bf16,
+ * and the up-projection merges the splits and multiplies in fp32.
  * Errors: MLA_ERR_NULL, MLA_ERR_ALIGN, MLA_ERR_SIZE (B < 1 or > 4096,
  * K < 1 or > 1<<20, S_cap < 1), MLA_ERR_WORKSPACE. */
 int mla_sparse_decode(const mla_bf16 *q_lat, const mla_bf16 *kv_cache, const mla_bf16 *pe_cache,

@@ -9,7 +9,10 @@
 // (K-major).  The latent outputs o arrive either as bf16 (written by the
 // attention kernel; loaded by TMA through a 3-D tensor map) or as fp32 (the
 // standalone entry point; rounded to bf16 while they are written into the
-// 128-byte-swizzled operand tile).
+// 128-byte-swizzled operand tile).  The one or two query rows of a split
+// selection are merged from the split partials and stay fp32: their product
+// with W_UV runs on the CUDA cores (a 16-column MMA pass is bound by the issue
+// of its 32 instructions).
 //
 // The kernel is launched as a programmatic dependent of the attention grid.
 // It loads W_UV before griddepcontrol.wait: the attention grid itself waits
@@ -65,8 +68,8 @@ __device__ __forceinline__ void stage_f32(const float *__restrict__ o_lat, int h
     }
 }
 
-// Split partials -> bf16 operand tile, for the one or two query rows of a
-// split selection: each row's latent output o is merged from its n_split
+// Split partials -> fp32 rows o_s [nb][512], for the one or two query rows of
+// a split selection: each row's latent output o is merged from its n_split
 // partials (normalised o of every split as bf16, and the log2 of each split's
 // softmax mass, one per latent half and head), o = sum_s 2^(lse_s - M) o_s /
 // sum_s 2^(lse_s - M) with M the largest lse_s, as the split-combine kernel
@@ -75,7 +78,7 @@ __device__ __forceinline__ void stage_f32(const float *__restrict__ o_lat, int h
 // columns of a row over the splits, with the loads of several splits in
 // flight at once.
 __device__ __forceinline__ void stage_partials(const uint16_t *__restrict__ part_o, const float *__restrict__ part_lse,
-                                               int n_split, int h, int n0, int nb, int N, uint8_t *sB, int tid,
+                                               int n_split, int h, int n0, int nb, float *o_s, int tid,
                                                float (*wts)[2][MERGE_SPLITS]) {
     const int warp = tid >> 5, lane = tid & 31;
     {
@@ -109,8 +112,8 @@ __device__ __forceinline__ void stage_partials(const uint16_t *__restrict__ part
         }
     }
     __syncthreads();
-    // piece q (4 latent columns) of row `row`: 128 per row, 8 bytes of partial and of the bf16 tile
-    for (int u = tid; u < N * 128; u += 128) {
+    // piece q (4 latent columns) of row `row`: 128 per row, 8 bytes of partial, 16 of the merged row
+    for (int u = tid; u < nb * 128; u += 128) {
         const int row = u >> 7, q = u & 127, half = q >= 64 ? 1 : 0;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row < nb) {
@@ -127,9 +130,7 @@ __device__ __forceinline__ void stage_partials(const uint16_t *__restrict__ part
                 a.z = fmaf(ws, bflo(v.y), a.z), a.w = fmaf(ws, bfhi(v.y), a.w);
             }
         }
-        const int ch = q >> 1;   // the 16-byte bf16 chunk (8 latent columns) this half-chunk belongs to
-        *reinterpret_cast<uint2 *>(sB + (ch >> 3) * B_ATOM + sw128(row, ch & 7) + (q & 1) * 8) =
-            make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
+        *reinterpret_cast<float4 *>(o_s + row * C + 4 * q) = a;
     }
 }
 
@@ -184,9 +185,51 @@ __global__ void __launch_bounds__(128, 1) out_up_kernel(const __grid_constant__ 
                 b_issued = pass + 1;
             }
         } else if (part_o) {
+            // one or two query rows from split partials: the merged rows stay fp32 and
+            // each thread takes one output feature d, a dot product of its W_UV row (in
+            // shared memory, 128B-swizzled boxes of 64 latent columns) with each row on
+            // the CUDA cores -- at N = 16 the 32 tensor-core MMAs are bound by their issue
+            // (about 1.5 us), the dot products take a fraction of that
             __shared__ float wts[MERGE_ROWS][2][MERGE_SPLITS];
-            stage_partials(part_o, part_lse, n_split, h, n0, nb, N, sB, tid, wts);
-            fence_proxy_async_smem();
+            __shared__ __align__(16) float o_s[MERGE_ROWS * C];
+            stage_partials(part_o, part_lse, n_split, h, n0, nb, o_s, tid, wts);
+            ok = __syncthreads_and(wait_until(&bars.a_full, 0, deadline));
+            if (!ok) break;
+            const int d = tid;
+            float acc[MERGE_ROWS];
+#pragma unroll
+            for (int rw = 0; rw < MERGE_ROWS; ++rw) acc[rw] = 0.f;
+#pragma unroll 1
+            for (int a = 0; a < 8; ++a) {   // box a: latent columns 64a .. 64a+63
+                const uint8_t *wr = sA + a * A_BOX + d * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {   // chunk j: columns 64a+8j .. 64a+8j+7
+                    const uint4 wv = *reinterpret_cast<const uint4 *>(wr + ((j ^ (d & 7)) << 4));
+                    const float w[8] = {bflo(wv.x), bfhi(wv.x), bflo(wv.y), bfhi(wv.y),
+                                        bflo(wv.z), bfhi(wv.z), bflo(wv.w), bfhi(wv.w)};
+#pragma unroll
+                    for (int rw = 0; rw < MERGE_ROWS; ++rw) {
+                        if (rw >= nb) break;
+                        const float4 o0 = *reinterpret_cast<const float4 *>(o_s + rw * C + 64 * a + 8 * j);
+                        const float4 o1 = *reinterpret_cast<const float4 *>(o_s + rw * C + 64 * a + 8 * j + 4);
+                        float s = acc[rw];
+                        s = fmaf(w[0], o0.x, s), s = fmaf(w[1], o0.y, s), s = fmaf(w[2], o0.z, s);
+                        s = fmaf(w[3], o0.w, s), s = fmaf(w[4], o1.x, s), s = fmaf(w[5], o1.y, s);
+                        s = fmaf(w[6], o1.z, s), s = fmaf(w[7], o1.w, s);
+                        acc[rw] = s;
+                    }
+                }
+            }
+#pragma unroll
+            for (int rw = 0; rw < MERGE_ROWS; ++rw) {
+                if (rw >= nb) break;
+                const size_t at = ((size_t)(n0 + rw) * H + h) * DV + d;
+                if (out_b16)
+                    out_b16[at] = f2bf(acc[rw]);
+                else
+                    out[at] = acc[rw];
+            }
+            continue;   // no tensor-core pass for these rows
         } else {
             stage_f32(o_f32, h, n0, nb, N, sB, tid);
             fence_proxy_async_smem();
